@@ -1,0 +1,122 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused attention forward.
+ *
+ * The operation ("Online softmax, and the register that can't move",
+ * section "Online softmax"; "Online Softmax: Tiling Across a Reduction",
+ * loop-order and statistics sections):
+ *
+ *     O   = softmax(Q K^T * scale) V          row by row, in one pass
+ *     LSE = m + ln(l)                          per query row
+ *
+ * computed key tile by key tile with a running row maximum m, a running sum
+ * of exponentials l and an output accumulator, each corrected by
+ * exp(m_old - m_new) when the maximum moves, and O divided by l once at the
+ * end.  The N x N score matrix never reaches device memory.  LSE (the
+ * natural-log normaliser) is the per-row statistic the backward pass needs
+ * ("Online Softmax: Tiling Across a Reduction", backward-pass section).
+ *
+ * Causal attention (key j visible to query i iff j <= i) skips key tiles
+ * that lie wholly after the query tile and masks element by element only on
+ * the diagonal tile ("Online Softmax: Tiling Across a Reduction", causal
+ * section).
+ *
+ * Layout (all contiguous, row-major, no padding):
+ *     q, k, v, o : bf16  [B][H][N][d]      (element (b,h,i,c) at ((b*H+h)*N+i)*d+c)
+ *     lse        : fp32  [B][H][N]
+ * Query and key sequences have the same length N.
+ *
+ * Ownership: every pointer is a DEVICE pointer owned by the caller.  The
+ * library allocates nothing per call, keeps no reference after returning,
+ * and never synchronises the host: the work is enqueued on `stream`
+ * (0 = the legacy default stream) and completes asynchronously.
+ *
+ * Errors: each entry point returns FA_OK (0) or a negative FA_ERR_* code;
+ * argument errors are detected on the host before anything is enqueued.
+ * fa_strerror() names a code.  A kernel that waits longer than its
+ * watchdog limit on an internal barrier abandons its tile, records a bit in
+ * a device status word and exits; fa_get_device_status() reads that word.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers */
+typedef struct CUstream_st* fa_stream_t;
+
+enum {
+    FA_OK = 0,
+    FA_ERR_NULL_POINTER = -1,   /* q, k, v, o or lse is NULL */
+    FA_ERR_HEAD_DIM = -2,       /* d is not 64 or 128 */
+    FA_ERR_SHAPE = -3,          /* B, H or N < 1, or B*H > 65535 */
+    FA_ERR_ALIGNMENT = -4,      /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
+    FA_ERR_SCALE = -5,          /* scale not finite or not > 0 */
+    FA_ERR_ALIAS = -6,          /* o or lse overlaps q, k or v, or each other */
+    FA_ERR_TENSOR_MAP = -7,     /* the driver rejected a TMA descriptor */
+    FA_ERR_CUDA = -8,           /* a CUDA runtime call failed (launch, attribute, driver entry point) */
+    FA_ERR_DEVICE = -9          /* the current device is not an sm_103 GPU */
+};
+
+/*
+ * fa_fwd -- fused attention forward.
+ *
+ *   q, k, v : device bf16 [B][H][N][d], 16-byte aligned, read only.
+ *   o       : device bf16 [B][H][N][d], 16-byte aligned, written.
+ *   lse     : device fp32 [B][H][N], written: ln(sum_j exp(scale * q_i . k_j))
+ *             over the visible keys j.
+ *   B, H    : batch and heads, >= 1, B*H <= 65535.
+ *   N       : sequence length >= 1 (any value; the last tile is masked).
+ *   d       : head dimension, 64 or 128.
+ *   causal  : nonzero masks key j > query i.
+ *   scale   : positive finite multiplier of the scores (1/sqrt(d) usually).
+ *   stream  : CUDA stream the work is enqueued on.
+ *
+ * Inputs are not modified.  o and lse must not overlap q, k, v or each other.
+ * Returns FA_OK once the kernel is enqueued.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           int causal, float scale, fa_stream_t stream);
+
+/* Human-readable name of an FA_* code; never NULL. */
+const char* fa_strerror(int code);
+
+/*
+ * Device status word of the current device: 0 when no kernel has given up
+ * on a barrier since the last fa_clear_device_status(); otherwise bit flags
+ * naming the wait that timed out.  Synchronises with the device.  Returns 0
+ * and stores the word in *status, or FA_ERR_CUDA.
+ */
+int fa_get_device_status(unsigned int* status);
+
+/* Reset the device status word of the current device to 0 (synchronous). */
+int fa_clear_device_status(void);
+
+/*
+ * Watchdog limit in nanoseconds applied to every barrier wait of later
+ * launches from this process (default 1e9).  Values below 1e6 are raised
+ * to 1e6.  Returns the previous value.
+ */
+uint64_t fa_set_watchdog_ns(uint64_t ns);
+
+/*
+ * Watchdog self-test: launches one CTA that waits on a shared-memory
+ * barrier no one arrives on, with a limit of `ns` nanoseconds, so the wait
+ * runs out.  The kernel records the timeout bit and returns; nothing faults
+ * or hangs.  Synchronises `stream` and stores the kernel's report in
+ * *status.  Returns FA_OK or FA_ERR_CUDA.
+ */
+int fa_watchdog_selftest(uint64_t ns, fa_stream_t stream, unsigned int* status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,149 @@
+"""GB300 (sm_103a) fused attention forward -- Python binding of include/fa.h.
+
+This module only marshals arguments: it turns tensors into device pointers
+and streams into handles and calls the C ABI in ``libfa_gb300.so``.  Every
+step of the computation runs in the CUDA kernels; there is no CPU or PyTorch
+fallback, and a missing library is an error.
+
+    fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream)   # C ABI mirror
+    o, lse = attention(q, k, v, causal=False, scale=None)         # allocates outputs
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "fa.h")
+
+FA_OK = 0
+FA_ERR_NULL_POINTER = -1
+FA_ERR_HEAD_DIM = -2
+FA_ERR_SHAPE = -3
+FA_ERR_ALIGNMENT = -4
+FA_ERR_SCALE = -5
+FA_ERR_ALIAS = -6
+FA_ERR_TENSOR_MAP = -7
+FA_ERR_CUDA = -8
+FA_ERR_DEVICE = -9
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what} (FA code {code})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; "
+                                   "g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            L.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P]
+            L.fa_fwd.restype = I
+            L.fa_strerror.argtypes = [I]
+            L.fa_strerror.restype = ctypes.c_char_p
+            L.fa_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+            L.fa_get_device_status.restype = I
+            L.fa_clear_device_status.argtypes = []
+            L.fa_clear_device_status.restype = I
+            L.fa_set_watchdog_ns.argtypes = [ctypes.c_uint64]
+            L.fa_set_watchdog_ns.restype = ctypes.c_uint64
+            L.fa_watchdog_selftest.argtypes = [ctypes.c_uint64, P, ctypes.POINTER(ctypes.c_uint)]
+            L.fa_watchdog_selftest.restype = I
+            L.fa_version.argtypes = []
+            L.fa_version.restype = I
+            _lib = L
+    return _lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_cuda:
+            raise ValueError("tensors must live on a CUDA device (no CPU path exists)")
+        if not x.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        return x.data_ptr()
+    raise TypeError(f"cannot take a device pointer from {type(x)!r}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fa_strerror(code: int) -> str:
+    return lib().fa_strerror(int(code)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, causal: bool, scale: float, stream=None) -> None:
+    """Enqueue the fused forward; raises FaError on a nonzero C return code."""
+    rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
+                      1 if causal else 0, float(scale), _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """q, k, v: CUDA bf16 [B, H, N, d].  Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N])."""
+    import torch
+
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("q, k and v must be bfloat16")
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, B, H, N, d, causal, (1.0 / math.sqrt(d)) if scale is None else scale, stream)
+    return o, lse
+
+
+def fa_get_device_status() -> int:
+    st = ctypes.c_uint(0)
+    rc = lib().fa_get_device_status(ctypes.byref(st))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+    return st.value
+
+
+def fa_clear_device_status() -> None:
+    rc = lib().fa_clear_device_status()
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+
+
+def fa_set_watchdog_ns(ns: int) -> int:
+    return int(lib().fa_set_watchdog_ns(int(ns)))
+
+
+def fa_watchdog_selftest(ns: int, stream=None) -> int:
+    st = ctypes.c_uint(0)
+    rc = lib().fa_watchdog_selftest(int(ns), _stream(stream), ctypes.byref(st))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+    return st.value
+
+
+def fa_version() -> int:
+    return int(lib().fa_version())

@@ -1,0 +1,182 @@
+// fa_fwd.cu -- host side of the C ABI declared in include/fa.h: argument
+// validation, TMA descriptor encoding and the kernel launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kMaxDevices = 64;
+
+uint64_t g_watchdog_ns = 1000000000ull;  // 1 s
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_device_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return g_encode;
+}
+
+int check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+    if (g_device_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_device_ok[dev] == 1 ? FA_OK : FA_ERR_DEVICE;
+}
+
+// [B*H][N][d] bf16 viewed as a 3-D tensor (d, N, B*H); box = one 128-row x
+// 64-column chunk, 128-byte swizzle.  Rows past N read as zero (loads) and
+// are dropped (stores), per head.
+bool encode_bhnd(CUtensorMap* m, const void* base, int d, int N, int BH) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2u, (cuuint64_t)N * (cuuint64_t)d * 2u};
+    cuuint32_t box[3] = {64u, 128u, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+template <int D, int NK, int NV>
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+           const fa::FaParams& p, int BH, cudaStream_t stream) {
+    using L = fa::FaSmem<D, NK, NV>;
+    auto kern = fa::fa_fwd_sm103<D, NK, NV>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
+        return FA_ERR_CUDA;
+    dim3 grid((unsigned)p.n_tiles, (unsigned)BH, 1);
+    kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, to, p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
+           float scale, fa_stream_t stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
+    if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+    const long long BH = (long long)B * (long long)H;
+    if (BH > 65535) return FA_ERR_SHAPE;
+    auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+    if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        return FA_ERR_ALIGNMENT;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+    const size_t tensor_bytes = (size_t)BH * (size_t)N * (size_t)d * 2u;
+    const size_t lse_bytes = (size_t)BH * (size_t)N * 4u;
+    if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
+        overlaps(o, tensor_bytes, v, tensor_bytes) || overlaps(lse, lse_bytes, q, tensor_bytes) ||
+        overlaps(lse, lse_bytes, k, tensor_bytes) || overlaps(lse, lse_bytes, v, tensor_bytes) ||
+        overlaps(lse, lse_bytes, o, tensor_bytes))
+        return FA_ERR_ALIAS;
+    const int dev_rc = check_device();
+    if (dev_rc != FA_OK) return dev_rc;
+
+    CUtensorMap tq, tk, tv, to;
+    if (!encode_bhnd(&tq, q, d, N, (int)BH) || !encode_bhnd(&tk, k, d, N, (int)BH) ||
+        !encode_bhnd(&tv, v, d, N, (int)BH) || !encode_bhnd(&to, o, d, N, (int)BH))
+        return FA_ERR_TENSOR_MAP;
+
+    fa::FaParams p;
+    p.lse = lse;
+    p.N = N;
+    p.n_tiles = (N + fa::kBlockN - 1) / fa::kBlockN;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * 1.44269504088896340736f;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        p.watchdog_ns = g_watchdog_ns;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d == 64) return launch<64, 4, 4>(tq, tk, tv, to, p, (int)BH, s);
+    return launch<128, 2, 2>(tq, tk, tv, to, p, (int)BH, s);
+}
+
+const char* fa_strerror(int code) {
+    switch (code) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL_POINTER: return "a tensor pointer is NULL";
+        case FA_ERR_HEAD_DIM: return "head dimension must be 64 or 128";
+        case FA_ERR_SHAPE: return "B, H and N must be >= 1 and B*H <= 65535";
+        case FA_ERR_ALIGNMENT: return "q, k, v, o must be 16-byte aligned and lse 4-byte aligned";
+        case FA_ERR_SCALE: return "scale must be positive and finite";
+        case FA_ERR_ALIAS: return "o or lse overlaps an input or each other";
+        case FA_ERR_TENSOR_MAP: return "the driver rejected a TMA tensor map";
+        case FA_ERR_CUDA: return "a CUDA runtime call failed";
+        case FA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+        default: return "unknown error code";
+    }
+}
+
+int fa_get_device_status(unsigned int* status) {
+    if (!status) return FA_ERR_NULL_POINTER;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(status, fa::g_fa_status, sizeof(unsigned int)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+int fa_clear_device_status(void) {
+    const unsigned int zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return cudaDeviceSynchronize() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+uint64_t fa_set_watchdog_ns(uint64_t ns) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const uint64_t old = g_watchdog_ns;
+    g_watchdog_ns = ns < 1000000ull ? 1000000ull : ns;
+    return old;
+}
+
+int fa_watchdog_selftest(uint64_t ns, fa_stream_t stream, unsigned int* status) {
+    if (!status) return FA_ERR_NULL_POINTER;
+    const int dev_rc = check_device();
+    if (dev_rc != FA_OK) return dev_rc;
+    if (fa_clear_device_status() != FA_OK) return FA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    fa::fa_watchdog_selftest_kernel<<<1, 32, 0, s>>>((unsigned long long)ns);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+    return fa_get_device_status(status);
+}
+
+int fa_version(void) { return kVersion; }
+
+}  // extern "C"

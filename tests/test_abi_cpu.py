@@ -1,0 +1,92 @@
+"""The C-ABI library: it loads, exports every function include/fa.h declares,
+and rejects bad arguments on the host before any CUDA work (no GPU needed)."""
+import ctypes
+import re
+
+import pytest
+import torch
+
+import __graft_entry__
+
+
+@pytest.fixture(scope="module")
+def fa():
+    __graft_entry__.build()
+    import online_softmax_04_gb300 as m
+
+    return m
+
+
+def declared_functions(path):
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)
+
+
+def test_exports_every_declared_symbol(fa):
+    names = declared_functions(fa.HEADER_PATH)
+    assert {"fa_fwd", "fa_strerror", "fa_get_device_status", "fa_clear_device_status", "fa_set_watchdog_ns",
+            "fa_watchdog_selftest", "fa_version"} <= set(names)
+    raw = ctypes.CDLL(fa.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_strerror_and_version(fa):
+    assert fa.fa_version() >= 10000
+    for code in range(-9, 1):
+        assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown error code"
+    assert fa.fa_strerror(-1000) == "unknown error code"
+
+
+FAKE = 1 << 40  # never dereferenced: every case below fails validation first
+
+
+def call(fa, q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), o=FAKE + (3 << 30), lse=FAKE + (4 << 30), B=1, H=1,
+         N=128, d=64, causal=0, scale=0.125):
+    return fa.lib().fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, 0)
+
+
+def test_host_validation(fa):
+    assert call(fa, q=0) == fa.FA_ERR_NULL_POINTER
+    assert call(fa, lse=0) == fa.FA_ERR_NULL_POINTER
+    assert call(fa, d=96) == fa.FA_ERR_HEAD_DIM
+    assert call(fa, d=256) == fa.FA_ERR_HEAD_DIM
+    assert call(fa, N=0) == fa.FA_ERR_SHAPE
+    assert call(fa, B=0) == fa.FA_ERR_SHAPE
+    assert call(fa, B=300, H=300) == fa.FA_ERR_SHAPE
+    assert call(fa, q=FAKE + 8) == fa.FA_ERR_ALIGNMENT
+    assert call(fa, lse=FAKE + (4 << 30) + 2) == fa.FA_ERR_ALIGNMENT
+    assert call(fa, scale=0.0) == fa.FA_ERR_SCALE
+    assert call(fa, scale=-1.0) == fa.FA_ERR_SCALE
+    assert call(fa, scale=float("nan")) == fa.FA_ERR_SCALE
+    assert call(fa, scale=float("inf")) == fa.FA_ERR_SCALE
+    assert call(fa, o=FAKE + 64) == fa.FA_ERR_ALIAS          # o overlaps q
+    assert call(fa, lse=FAKE + (3 << 30) + 64) == fa.FA_ERR_ALIAS  # lse overlaps o
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="valid arguments would launch on a real GPU")
+def test_valid_arguments_without_a_gpu_fail_cleanly(fa):
+    rc = call(fa)
+    assert rc in (fa.FA_ERR_CUDA, fa.FA_ERR_DEVICE)
+
+
+def test_binding_refuses_cpu_tensors(fa):
+    q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.attention(q, q, q)
+
+
+def test_product_does_not_import_the_oracle():
+    import os
+
+    import online_softmax_04_gb300
+
+    pkg = os.path.dirname(online_softmax_04_gb300.__file__)
+    for name in os.listdir(pkg):
+        if name.endswith((".py", ".cu", ".cuh")):
+            src = open(os.path.join(pkg, name)).read()
+            assert "import oracle" not in src and "from oracle" not in src and "liboracle" not in src, name
+    for name in os.listdir(os.path.join(pkg, "csrc")):
+        src = open(os.path.join(pkg, "csrc", name)).read()
+        assert "oracle" not in src, name

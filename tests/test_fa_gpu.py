@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA path against the fp64 CPU oracle on the same seeded
+inputs, element by element.
+
+Tolerances (bf16 inputs, fp32 accumulation, bf16 output): max |O_gpu - O_ref|
+<= 2e-2 over every checked element, and |LSE_gpu - LSE_ref| / max(1, |LSE_ref|)
+<= 1e-3 per checked row.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from online_softmax_04_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import online_softmax_04_gb300 as m
+
+    m.fa_clear_device_status()
+    yield m
+    assert m.fa_get_device_status() == 0, "a kernel gave up on a barrier"
+
+
+def run_gpu(fa, q, k, v, causal, scale):
+    dev = torch.device("cuda:0")
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def compare(o_gpu, lse_gpu, q, k, v, causal, scale, rows, label=""):
+    B, H, N, d = q.shape
+    ref_o, ref_lse = oracle.attention_three_pass(q, k, v, causal, scale, rows=rows)
+    got_o = o_gpu.reshape(-1, d)[rows].astype(np.float64)
+    got_lse = lse_gpu.reshape(-1)[rows].astype(np.float64)
+    assert np.all(np.isfinite(got_o)) and np.all(np.isfinite(got_lse)), f"{label}: non-finite output"
+    err_o = np.abs(got_o - ref_o)
+    err_l = np.abs(got_lse - ref_lse) / np.maximum(1.0, np.abs(ref_lse))
+    worst = int(np.argmax(err_o.max(axis=1)))
+    msg = (f"{label}: max|dO|={err_o.max():.3e} (row {rows[worst]}) max rel dLSE={err_l.max():.3e} "
+           f"rows={len(rows)}")
+    print(msg)
+    assert err_o.max() <= O_TOL, msg
+    assert err_l.max() <= LSE_TOL, msg
+    return err_o.max(), err_l.max()
+
+
+def all_rows(B, H, N):
+    return np.arange(B * H * N, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# small shapes: every row, ragged tails, both head dims, both mask modes
+# --------------------------------------------------------------------------
+SMALL = [
+    (1, 1, 1, 64, False), (1, 1, 1, 128, True), (1, 2, 7, 64, True), (2, 1, 100, 128, False),
+    (1, 1, 128, 64, False), (1, 1, 128, 128, True), (1, 1, 129, 128, True), (1, 1, 129, 64, False),
+    (1, 1, 255, 64, True), (1, 2, 300, 128, True), (2, 2, 384, 64, False), (1, 1, 1000, 128, True),
+    (1, 1, 1000, 64, False), (3, 5, 520, 64, True),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL)
+def test_small_shapes_every_row(fa, B, H, N, d, causal):
+    w = wl.Workload("small", B, H, N, d, causal, "iid", 100 + N + d)
+    q, k, v = wl.make_inputs(w)
+    o, lse = run_gpu(fa, q, k, v, causal, w.scale)
+    compare(o, lse, q, k, v, causal, w.scale, all_rows(B, H, N), f"B{B} H{H} N{N} d{d} causal={causal}")
+
+
+@pytest.mark.parametrize("name", [
+    "B1-H1-N256-d64-full", "B1-H1-N256-d64-full-sorted", "B1-H1-N256-d64-full-sorted-strict",
+    "B1-H1-N4096-d64-full",
+])
+def test_small_workloads_every_row(fa, name):
+    w = wl.WORKLOADS[name]
+    q, k, v = wl.make_inputs(w)
+    o, lse = run_gpu(fa, q, k, v, w.causal, w.scale)
+    compare(o, lse, q, k, v, w.causal, w.scale, wl.sample_rows(w), name)
+
+
+@pytest.mark.parametrize("name", [
+    "B4-H16-N4096-d128-causal", "B1-H32-N16384-d128-causal-late", "B1-H8-N131072-d64-causal",
+])
+def test_large_workloads_sampled_rows(fa, name):
+    w = wl.WORKLOADS[name]
+    q, k, v = wl.make_inputs(w)
+    o, lse = run_gpu(fa, q, k, v, w.causal, w.scale)
+    compare(o, lse, q, k, v, w.causal, w.scale, wl.sample_rows(w), name)
+
+
+# --------------------------------------------------------------------------
+# closed forms that hold at any size
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d,c", [(64, 64, 18.0), (128, 128, 22.0)])
+def test_onehot_dominant_key(fa, causal, N, d, c):
+    q, k, v = wl.onehot_inputs(2, 3, N, d, c)
+    scale = 1 / math.sqrt(d)
+    s = scale * c * c
+    o, lse = run_gpu(fa, q, k, v, causal, scale)
+    vd = v.float().numpy().astype(np.float64)
+    bound = (N - 1) * math.exp(-s) * 2 * np.abs(vd).max() + np.abs(vd).max() * 2.0 ** -8
+    assert np.max(np.abs(o - vd)) <= bound
+    n_vis = np.arange(1, N + 1) if causal else np.full(N, N)
+    want_lse = s + np.log1p((n_vis - 1) * math.exp(-s))
+    assert np.max(np.abs(lse - want_lse[None, None, :]) / np.maximum(1, want_lse)) <= LSE_TOL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(8192, 64), (3000, 128)])
+def test_uniform_attention_any_size(fa, causal, N, d):
+    """q = 0: every visible key weighs the same, so O is a (prefix) mean of V and LSE = ln(#visible)."""
+    w = wl.Workload("zeros", 1, 2, N, d, causal, "zeros-q", 77)
+    q, k, v = wl.make_inputs(w)
+    o, lse = run_gpu(fa, q, k, v, causal, w.scale)
+    vd = v.float().numpy().astype(np.float64)[0]
+    if causal:
+        want = np.cumsum(vd, axis=1) / np.arange(1, N + 1)[None, :, None]
+        want_lse = np.log(np.arange(1, N + 1))
+    else:
+        want = np.broadcast_to(vd.mean(axis=1, keepdims=True), vd.shape)
+        want_lse = np.full(N, math.log(N))
+    assert np.max(np.abs(o[0] - want)) <= O_TOL
+    assert np.max(np.abs(lse[0] - want_lse[None]) / np.maximum(1, want_lse[None])) <= LSE_TOL
+
+
+# --------------------------------------------------------------------------
+# behaviour of the boundary
+# --------------------------------------------------------------------------
+def test_deterministic_and_stream(fa):
+    w = wl.Workload("det", 2, 3, 700, 128, True, "iid", 5)
+    q, k, v = (t.cuda() for t in wl.make_inputs(w))
+    o1, l1 = fa.attention(q, k, v, causal=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o2, l2 = fa.attention(q, k, v, causal=True, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_inputs_untouched(fa):
+    w = wl.Workload("ro", 1, 2, 300, 64, False, "iid", 6)
+    q, k, v = (t.cuda() for t in wl.make_inputs(w))
+    qc, kc, vc = q.clone(), k.clone(), v.clone()
+    fa.attention(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(q, qc) and torch.equal(k, kc) and torch.equal(v, vc)
+
+
+def test_rejects_bad_arguments_on_device(fa):
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
+    L = fa.lib()
+    ptr = q.data_ptr()
+    assert L.fa_fwd(ptr, ptr, ptr, o.data_ptr(), lse.data_ptr(), 1, 1, 128, 96, 0, 0.1, 0) == fa.FA_ERR_HEAD_DIM
+    assert L.fa_fwd(ptr + 2, ptr, ptr, o.data_ptr(), lse.data_ptr(), 1, 1, 128, 64, 0, 0.1, 0) == fa.FA_ERR_ALIGNMENT
+    assert L.fa_fwd(ptr, ptr, ptr, ptr, lse.data_ptr(), 1, 1, 128, 64, 0, 0.1, 0) == fa.FA_ERR_ALIAS
+    assert L.fa_fwd(ptr, ptr, ptr, o.data_ptr(), lse.data_ptr(), 1, 1, 128, 64, 0, -1.0, 0) == fa.FA_ERR_SCALE
+    with pytest.raises(ValueError):
+        fa.attention(q.cpu(), q.cpu(), q.cpu())
+
+
+def test_watchdog_ends_a_wait_nothing_completes(fa):
+    st = fa.fa_watchdog_selftest(20_000_000)  # 20 ms limit on a barrier no one arrives on
+    assert st & (1 << 8), f"status {st:#x}"
+    fa.fa_clear_device_status()
+    assert fa.fa_get_device_status() == 0
+    # the context is still usable afterwards
+    w = wl.Workload("after", 1, 1, 256, 64, True, "iid", 8)
+    q, k, v = wl.make_inputs(w)
+    o, lse = run_gpu(fa, q, k, v, True, w.scale)
+    compare(o, lse, q, k, v, True, w.scale, all_rows(1, 1, 256), "after watchdog")
