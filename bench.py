@@ -1,0 +1,375 @@
+#!/usr/bin/env python3
+"""Throughput of the fused attention forward on GB300.
+
+One step = one fused forward (S = Q K^T, online softmax, O = P V, O/l, LSE)
+over one batch of the workload, through the C ABI ``fa_fwd``.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line.  ``value`` is whole-job TFLOP/s with inputs resident in
+device memory, timed with CUDA events on the launching stream; FLOPs per step
+are 4 B H N^2 d, halved for causal attention.  ``e2e`` is the same metric with
+the pinned-host -> device copies of Q, K, V and the device -> host copies of
+O and LSE inside the timed region.  ``--impl reference`` times the fp64 CPU
+oracle (three-pass route) on the host cores on a bounded sample of rows.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the whole workload on
+its own seeded inputs (independent problems, no collective on the data path),
+so scaling is weak; timing is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 tensor peak"
+FALLBACK_BF16_TFLOPS = 1900.0  # used only when MEASURED_PEAKS.json is absent
+KERNEL_NAME = "fa_fwd_sm103"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def workload_flops(w) -> float:
+    f = 4.0 * w.B * w.H * float(w.N) ** 2 * w.d
+    return f / 2 if w.causal else f
+
+
+def row_flops(w, rows) -> float:
+    """The metric's FLOPs attributable to the given query rows: 4 d per visible key."""
+    import numpy as np
+
+    i = np.asarray(rows) % w.N
+    n_vis = (i + 1) if w.causal else np.full(len(i), w.N)
+    return float(4.0 * w.d * n_vis.sum())
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "online_softmax_04_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 3 and parts[0] == workload and parts[1] == want:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        self.out.flush()
+        self.out.seek(0)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, mx, power = float(f[1]), float(f[2]), float(f[3])
+            except ValueError:
+                continue
+            if power < 200:  # idle sample, before or after the kernels
+                continue
+            sms.append(sm)
+            maxes.append(mx)
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.out.name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def cpu_baseline(w, q, k, v, target_s: float = 10.0):
+    """Time the fp64 oracle on the host cores over a bounded sample of query rows."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(w.seed + 99)
+    total = w.B * w.H * w.N
+    perm = rng.permutation(total) if total <= 50_000_000 else rng.integers(0, total, size=1_000_000)
+    n0 = min(256, total)
+    t0 = time.perf_counter()
+    oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=perm[:n0])
+    t_cal = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(len(perm), max(n0, n0 * target_s / t_cal)))
+    rows = perm[:n]
+    t0 = time.perf_counter()
+    _, _, used = oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=rows, return_threads=True)
+    dt = time.perf_counter() - t0
+    return {"value": row_flops(w, rows) / dt / 1e12, "unit": "TFLOP/s", "cores": int(used), "kind": "oracle",
+            "sample": f"{n} seeded query rows of {w.name} (of {total}), fp64 three-pass route, {dt:.1f} s"}
+
+
+def run_reference(args, w, rank, world):
+    """The oracle as the reference arm: K timed steps, each a bounded row sample."""
+    if rank != 0:
+        return
+    from online_softmax_04_gb300 import workloads as wl
+
+    q, k, v = wl.make_inputs(w)
+    per_step_s = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(w.seed + 5)
+    total = w.B * w.H * w.N
+    t0 = time.perf_counter()
+    oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=rng.integers(0, total, 128))
+    t_cal = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(128, 128 * per_step_s / t_cal))
+    flops, secs, used = 0.0, 0.0, 1
+    for step in range(args.warmup + args.steps):
+        rows = rng.integers(0, total, n)
+        t0 = time.perf_counter()
+        _, _, used = oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=rows, return_threads=True)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            flops += row_flops(w, rows)
+            secs += dt
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": int(used), "kind": "oracle",
+                         "sample": f"{n} random query rows per step of {w.name}, fp64 three-pass route"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling captures)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+
+    from online_softmax_04_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[args.workload or wl.HEADLINE]
+    if args.heads:
+        w = w.with_(H=args.heads, name=f"{w.name}@H{args.heads}")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    if local_rank == 0:
+        __graft_entry__.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+        dist.barrier()
+        if local_rank != 0:
+            __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    import online_softmax_04_gb300 as fa
+
+    # every rank solves its own problem: same shapes, its own seed
+    wr = w.with_(seed=w.seed + 1000 * rank)
+    q, k, v = wl.make_inputs(wr)
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(dq)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_fwd(dq, dk, dv, o, lse, w.B, w.H, w.N, w.d, w.causal, w.scale, stream)
+
+    fa.fa_clear_device_status()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # Inputs and outputs larger than L2 make back-to-back steps honest; smaller
+    # workloads get L2 flushed (a 512 MB write) before each individually timed step.
+    io_bytes = 4 * q.numel() * q.element_size() + lse.numel() * lse.element_size()
+    flush_l2 = io_bytes < 2 * L2_BYTES
+    scratch = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush_l2 else None
+
+    def timed(fn, n):
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if flush_l2:
+            ms = 0.0
+            for _ in range(n):
+                scratch.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ms += e0.elapsed_time(e1)
+        else:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+            dist.barrier()
+        return ms
+
+    with ClockSampler(local_rank) as clk:
+        ms_total = timed(step, args.steps)
+    clocks = clk.summary()
+    ms_step = ms_total / args.steps
+    flops = workload_flops(w)
+    value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+
+    # end to end: pinned host buffers, copies inside the timed region
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.fa_fwd(dq, dk, dv, o, lse, w.B, w.H, w.N, w.d, w.causal, w.scale, stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    ms_e2e = timed(e2e_step, args.steps)
+    e2e_value = world * flops * args.steps / (ms_e2e * 1e-3) / 1e12
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    status = fa.fa_get_device_status()
+    if status != 0:
+        raise SystemExit(f"device status word {status:#x}: a kernel gave up on a barrier")
+
+    if rank == 0:
+        peak, peak_src = measured_peak()
+        achieved = flops / (ms_step * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": recorded_traffic(w.name), "peak_source": peak_src,
+                    "kernel": KERNEL_NAME}
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(w, q, k, v)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                       "scale": "1/sqrt(d)", "flops_per_step_per_gpu": flops,
+                       "l2": ("L2 flushed (512 MB write) before each individually timed step" if flush_l2 else
+                              f"inputs larger than L2 ({io_bytes / 2**20:.0f} MiB of Q, K, V, O, LSE > 129 MB), "
+                              "back-to-back steps, no flush"),
+                       "parallelism": f"independent problem per GPU x{world}"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": ms_e2e / args.steps},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

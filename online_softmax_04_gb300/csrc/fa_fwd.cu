@@ -78,6 +78,8 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
     auto kern = fa::fa_fwd_sm103<D, NK, NV>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
         return FA_ERR_CUDA;
+    // one CTA per 128-row query tile; blockIdx.x runs from the last (longest
+    // causal) tile down, so the heaviest CTAs are scheduled first
     dim3 grid((unsigned)p.n_tiles, (unsigned)BH, 1);
     kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -124,8 +126,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         p.watchdog_ns = g_watchdog_ns;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (d == 64) return launch<64, 4, 4>(tq, tk, tv, to, p, (int)BH, s);
-    return launch<128, 2, 2>(tq, tk, tv, to, p, (int)BH, s);
+    if (d == 64) return launch<64, 6, 6>(tq, tk, tv, to, p, (int)BH, s);
+    return launch<128, 3, 3>(tq, tk, tv, to, p, (int)BH, s);
 }
 
 const char* fa_strerror(int code) {

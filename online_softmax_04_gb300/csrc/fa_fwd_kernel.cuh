@@ -3,7 +3,7 @@
 // One CTA owns one 128-row query tile of one (batch, head) and streams the
 // key/value tiles past it ("Online Softmax: Tiling Across a Reduction", loop
 // order: query blocks outer and resident, key/value blocks inner).  Per key
-// tile j the running row state is updated with one correction factor
+// tile j each query row updates its state with one correction factor
 // ("Online softmax, and the register that can't move", section "Online
 // softmax"):
 //
@@ -12,20 +12,34 @@
 //     O_new = O_old * exp(m_old - m_new) + exp(S_j - m_new) V_j
 //
 // and after the last tile O /= l, LSE = m + ln l.  Scores are kept in the
-// base-2 domain: t = s * scale * log2(e), so every exponential is one ex2.
+// base-2 domain, t = s * scale * log2(e), so every exponential is one ex2.
 //
 // GB300 mapping:
 //   * S_j = Q K_j^T and O += P_j V_j run on tcgen05.mma (bf16 in, fp32
-//     accumulate) with the accumulators in tensor memory (TMEM): S is double
-//     buffered so S_{j+1} is computed while the softmax works on S_j.
+//     accumulate) with the accumulators in tensor memory (TMEM).  S is double
+//     buffered and P has columns of its own, so S_{j+1} is computed while the
+//     softmax works on S_j and nothing waits for a product to drain.
+//   * Two MMA-issuing warps: one issues the S products as soon as a K tile
+//     and an S buffer are free, the other the P V products as soon as P_j is
+//     written.  A tcgen05.mma burst keeps its issuing thread busy until the
+//     tensor pipe has taken it, so two issuers keep the pipe fed while either
+//     one waits on a barrier.
 //   * P_j is written back to TMEM as bf16 and consumed from there as the A
-//     operand of the P V product (no shared-memory round trip).
-//   * Q, K_j and V_j are brought in by TMA (128-byte swizzle) into a ring of
+//     operand of P V (no shared-memory round trip).
+//   * Q, K_j and V_j are brought in by TMA (128-byte swizzle) into rings of
 //     shared-memory stages guarded by mbarriers.
-//   * Warp roles: warp 0 issues TMA loads, warp 1 owns TMEM and issues the
-//     MMAs, warps 2-5 (one thread per query row) do the softmax, the O
-//     rescale on TMEM and the epilogue (O/l -> bf16 -> shared -> TMA store,
-//     LSE store).
+//   * Warp roles: warp 0 issues TMA loads, warp 1 owns TMEM and issues the S
+//     products, warp 2 issues the P V products, warps 4-7 (one thread per
+//     query row) do the softmax, the O rescale on TMEM and the epilogue
+//     (O/l -> bf16 -> shared -> TMA store, LSE store).
+//   * The reference maximum of a row moves only when the row maximum has
+//     grown past it by more than 64 in base-2 units; otherwise the old
+//     reference is kept, exponentials up to 2^64 are accumulated in fp32 and
+//     the O rescale on TMEM is skipped.  exp(x - m) / sum exp(x - m) does not
+//     depend on m, so the result is unchanged.
+//   * O is divided by the sum of the bf16-rounded exponentials, the very
+//     weights the P V product uses, so O / l is a convex combination of V
+//     rows; LSE uses the fp32 sum of the unrounded exponentials.
 //   * Causal: key tiles wholly after the query tile are never visited; only
 //     the diagonal tile is masked element by element ("Online Softmax: Tiling
 //     Across a Reduction", causal section).  Keys >= N in the last tile are
@@ -42,10 +56,14 @@ namespace fa {
 
 constexpr int kBlockM = 128;   // query rows per tile = TMEM lanes
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 256;  // 8 warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kChunkBytes = 128u * 128u;  // one [128 rows][64 bf16] swizzled chunk
 constexpr float kLn2 = 0.69314718055994530942f;
+// Base-2 growth of a row's maximum tolerated before its reference moves.  It
+// bounds every exponential by 2^64, the row sums by N * 2^64 and |O| by
+// N * 2^64 * max|V|: finite in fp32 for max|V| < 2^33 at any N < 2^31.
+constexpr float kRescaleThreshold = 64.0f;
 
 // device status bits (which wait ran out)
 enum : unsigned int {
@@ -55,9 +73,11 @@ enum : unsigned int {
     kStatusMmaWaitP = 1u << 3,
     kStatusMmaWaitV = 1u << 4,
     kStatusSoftmaxWaitS = 1u << 5,
-    kStatusSoftmaxWaitPV = 1u << 6,
+    kStatusSoftmaxWaitO = 1u << 6,
     kStatusDrain = 1u << 7,
     kStatusSelfTest = 1u << 8,
+    kStatusMmaWaitSFree = 1u << 9,
+    kStatusSoftmaxWaitPV = 1u << 10,
 };
 
 __device__ unsigned int g_fa_status = 0;
@@ -65,7 +85,7 @@ __device__ unsigned int g_fa_status = 0;
 struct FaParams {
     float* lse;
     int N;
-    int n_tiles;       // ceil(N / 128)
+    int n_tiles;       // ceil(N / 128) query (= key) tiles
     int causal;
     float scale_log2;  // scale * log2(e)
     unsigned long long watchdog_ns;
@@ -73,9 +93,10 @@ struct FaParams {
 
 template <int D, int NK, int NV>
 struct FaSmem {
+    static_assert(D == 64 || D == 128, "head dim");
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kTileBytes = kBlockN * D * 2;
-    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffQ = 0;  // the query tile, later the O staging
     static constexpr uint32_t kOffK = kOffQ + kTileBytes;
     static constexpr uint32_t kOffV = kOffK + NK * kTileBytes;
     static constexpr uint32_t kOffBar = kOffV + NV * kTileBytes;
@@ -84,23 +105,22 @@ struct FaSmem {
     static constexpr int kBarKEmpty = kBarKFull + NK;
     static constexpr int kBarVFull = kBarKEmpty + NK;
     static constexpr int kBarVEmpty = kBarVFull + NV;
-    static constexpr int kBarSFull = kBarVEmpty + NV;  // 2 buffers
-    static constexpr int kBarPFull = kBarSFull + 2;    // 2 buffers
-    static constexpr int kBarPV = kBarPFull + 2;
-    static constexpr int kBarDrain = kBarPV + 1;
-    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kBarSFull = kBarVEmpty + NV;  // per S buffer: S_j written
+    static constexpr int kBarSFree = kBarSFull + 2;    // per S buffer: S_j read by the softmax
+    static constexpr int kBarPFull = kBarSFree + 2;    // per P buffer: P_j written
+    static constexpr int kBarPVDone = kBarPFull + 2;   // per P buffer: P_j V_j finished
+    static constexpr int kBarOFinal = kBarPVDone + 2;  // the last P V product finished
+    static constexpr int kBarDrain = kBarOFinal + 1;   // per MMA issuer
+    static constexpr int kNumBars = kBarDrain + 2;
     static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
     static constexpr uint32_t kBytes = kOffAbort + 4;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
-    // TMEM columns
-    static constexpr uint32_t kColS0 = 0;
-    static constexpr uint32_t kColS1 = 128;
+    // TMEM columns: S0 S1 O P0 P1
+    __host__ __device__ static constexpr uint32_t col_s(int b) { return (uint32_t)b * 128u; }
     static constexpr uint32_t kColO = 256;
-    static constexpr uint32_t kColP0 = 256 + D;
-    static constexpr uint32_t kColP1 = 256 + D + 64;
-    static_assert(kColP1 + 64 <= kTmemCols, "TMEM budget");
-    static_assert(D == 64 || D == 128, "head dim");
+    __host__ __device__ static constexpr uint32_t col_p(int b) { return 256u + D + (uint32_t)b * 64u; }
+    static_assert(256 + D + 128 <= (int)kTmemCols, "TMEM budget");
 };
 
 // Bounded wait on an mbarrier phase.  Gives up when another warp of the CTA
@@ -145,6 +165,30 @@ __device__ __forceinline__ bool fa_wait_drain(uint32_t bar, uint32_t parity, uin
     }
 }
 
+// Exponentials of one 128-key row tile against the reference -neg_m (base 2):
+// P packed to bf16 pairs, the sum of the bf16-rounded values and the fp32 sum.
+__device__ __forceinline__ void exp_row_tile(const float (&s)[kBlockN], float c2, float neg_m,
+                                             uint32_t (&pk)[kBlockN / 2], float& sum_bf, float& sum_f32) {
+    const uint64_t c2x2 = f32x2_pack(c2, c2), negm2 = f32x2_pack(neg_m, neg_m);
+    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+    uint64_t r32[2] = {0ull, 0ull};  // packed (even, odd) fp32 partial sums
+#pragma unroll
+    for (int i = 0; i < kBlockN / 2; ++i) {
+        float x0, x1;
+        f32x2_unpack(ffma2(f32x2_pack(s[2 * i], s[2 * i + 1]), c2x2, negm2), x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        pk[i] = pack_bf16x2(p0, p1);
+        rs[i & 3] = add_bf16x2_f32(rs[i & 3], pk[i]);
+        r32[i & 1] = fadd2(r32[i & 1], f32x2_pack(p0, p1));
+    }
+    float e0, e1, o0, o1;
+    f32x2_unpack(r32[0], e0, o0);
+    f32x2_unpack(r32[1], e1, o1);
+    sum_bf = (rs[0] + rs[1]) + (rs[2] + rs[3]);
+    sum_f32 = (e0 + o0) + (e1 + o1);
+}
+
 template <int D, int NK, int NV>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -162,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = (int)(threadIdx.x & 31);
     const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest causal rows first
     const int bh = (int)blockIdx.y;
-    const int n_kv = p.causal ? (qt + 1) : p.n_tiles;
+    const int n_kv = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;
     const uint64_t limit = p.watchdog_ns;
 
     if (warp == 0 && lane == 0) {
@@ -180,10 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::kBarSFull + b), 1);
-            mbar_init(bar(L::kBarPFull + b), 4);  // one arrival per softmax warp
+            mbar_init(bar(L::kBarSFree + b), 4);  // one arrival per softmax warp
+            mbar_init(bar(L::kBarPFull + b), 4);
+            mbar_init(bar(L::kBarPVDone + b), 1);
+            mbar_init(bar(L::kBarDrain + b), 1);
         }
-        mbar_init(bar(L::kBarPV), 1);
-        mbar_init(bar(L::kBarDrain), 1);
+        mbar_init(bar(L::kBarOFinal), 1);
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_q);
@@ -202,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------------
-        // TMA producer: Q once, then K_0, and K_{j+1} ahead of V_j, which is
-        // the order the MMA warp consumes them in.
+        // TMA producer: Q once; K_0, K_1; then V_j and K_{j+2}, the order in
+        // which the two MMA issuers consume them.
         // ------------------------------------------------------------------
         if (lane == 0) {
             mbar_arrive_expect_tx(bar(L::kBarQ), L::kTileBytes);
@@ -236,9 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             bool ok = load_k(0);
+            if (ok && n_kv > 1) ok = load_k(1);
             for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) ok = load_k(j + 1);
-                if (ok) ok = load_v(j);
+                ok = load_v(j);
+                if (ok && j + 2 < n_kv) ok = load_k(j + 2);
             }
             if (!ok) {
                 // abort: let every copy already issued land before the CTA exits
@@ -252,62 +299,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------------
-        // MMA issuer (one thread).  Order: S_0, S_1, then per j:
-        // [P_j ready] O += P_j V_j, S_{j+2}.
+        // S issuer: S_j = Q K_j^T into buffer j % 2 once K_j has landed and
+        // the softmax has read S_{j-2} out of that buffer.
         // ------------------------------------------------------------------
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+            const uint32_t qa = sbase + L::kOffQ;
             bool ok = fa_wait(bar(L::kBarQ), 0, abort_flag, limit, kStatusMmaWaitQ);
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % NK;
-                const uint32_t r = (uint32_t)(j / NK);
-                if (!fa_wait(bar(L::kBarKFull + s), r & 1u, abort_flag, limit, kStatusMmaWaitK)) return false;
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int b = j & 1;
+                const int ks = j % NK;
+                if (j >= 2)
+                    ok = fa_wait(bar(L::kBarSFree + b), (uint32_t)(((j - 2) >> 1) & 1), abort_flag, limit,
+                                 kStatusMmaWaitSFree);
+                ok = ok && fa_wait(bar(L::kBarKFull + ks), (uint32_t)((j / NK) & 1), abort_flag, limit,
+                                   kStatusMmaWaitK);
+                if (!ok) break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem + ((j & 1) ? L::kColS1 : L::kColS0);
-                const uint32_t qa = sbase + L::kOffQ;
-                const uint32_t ka = sbase + L::kOffK + s * L::kTileBytes;
+                const uint32_t ka = sbase + L::kOffK + (uint32_t)ks * L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(d_tmem, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdescS,
-                           kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + L::col_s(b), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                           kIdescS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(L::kBarKEmpty + s));
-                tc_commit(bar(L::kBarSFull + (j & 1)));
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && n_kv > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int b = j & 1;
-                if (!fa_wait(bar(L::kBarPFull + b), (uint32_t)((j >> 1) & 1), abort_flag, limit, kStatusMmaWaitP)) {
-                    ok = false;
-                    break;
-                }
-                const int s = j % NV;
-                const uint32_t r = (uint32_t)(j / NV);
-                if (!fa_wait(bar(L::kBarVFull + s), r & 1u, abort_flag, limit, kStatusMmaWaitV)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t va = sbase + L::kOffV + s * L::kTileBytes;
-                const uint32_t pa = tmem + (b ? L::kColP1 : L::kColP0);
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts(tmem + L::kColO, pa + (uint32_t)kk * 8u, sdesc_sw128(va + (uint32_t)kk * 2048u, kChunkBytes, 1024),
-                           kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar(L::kBarVEmpty + s));
-                tc_commit(bar(L::kBarPV));
-                if (j + 2 < n_kv) ok = issue_s(j + 2);
+                tc_commit(bar(L::kBarSFull + b));
+                tc_commit(bar(L::kBarKEmpty + ks));
             }
-            // every MMA must finish before TMEM is released
-            tc_commit(bar(L::kBarDrain));
-            fa_wait_drain(bar(L::kBarDrain), 0, limit);
+            tc_commit(bar(L::kBarDrain + 0));  // every MMA must finish before TMEM is released
+            fa_wait_drain(bar(L::kBarDrain + 0), 0, limit);
         }
         __syncwarp();
-    } else {
+    } else if (warp == 2) {
+        // ------------------------------------------------------------------
+        // P V issuer: O += P_j V_j once P_j is in TMEM and V_j has landed.
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+            bool ok = true;
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int b = j & 1;
+                const int vs = j % NV;
+                ok = fa_wait(bar(L::kBarPFull + b), (uint32_t)((j >> 1) & 1), abort_flag, limit, kStatusMmaWaitP) &&
+                     fa_wait(bar(L::kBarVFull + vs), (uint32_t)((j / NV) & 1), abort_flag, limit, kStatusMmaWaitV);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t va = sbase + L::kOffV + (uint32_t)vs * L::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u,
+                           sdesc_sw128(va + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescPV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar(L::kBarVEmpty + vs));
+                tc_commit(bar(L::kBarPVDone + b));
+                if (j + 1 == n_kv) tc_commit(bar(L::kBarOFinal));
+            }
+            tc_commit(bar(L::kBarDrain + 1));
+            fa_wait_drain(bar(L::kBarDrain + 1), 0, limit);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
         // ------------------------------------------------------------------
         // Softmax / correction / epilogue: thread = one query row = TMEM lane.
         // ------------------------------------------------------------------
@@ -316,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q_idx = qt * kBlockM + row;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         const float c2 = p.scale_log2;
-        float m_run = -INFINITY;  // running max, base-2 scaled units
-        float l_run = 0.f;        // running sum of 2^(t - m_run)
+        float m_run = -INFINITY;  // reference max, base-2 scaled units
+        float l_run = 0.f;        // sum of bf16(2^(t - m_run)): normalises O
+        float l32_run = 0.f;      // sum of 2^(t - m_run) in fp32: gives LSE
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const int b = j & 1;
@@ -329,15 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             float s[kBlockN];
             {
-                const uint32_t scol = t_lane + (b ? L::kColS1 : L::kColS0);
+                uint32_t r[kBlockN];
+                tmem_ld128_wait(t_lane + L::col_s(b), r);
 #pragma unroll
-                for (int c = 0; c < kBlockN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32_wait(scol + 32u * c, r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
-                }
+                for (int i = 0; i < kBlockN; ++i) s[i] = __uint_as_float(r[i]);
             }
+            // S_j is in registers: the buffer may take S_{j+2}
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarSFree + b));
             // mask keys past the diagonal (causal) and past the end of the sequence
             int lim = p.N - 1 - j * kBlockN;
             if (p.causal && j == qt) lim = min(lim, row);
@@ -345,53 +397,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kBlockN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
             }
-            // tile row max (scale > 0, so max(s) * c2 == max(s * c2))
-            float mx[4] = {s[0], s[1], s[2], s[3]};
+            float mx[4] = {fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), fmax3(s[6], s[7], s[8]),
+                           fmax3(s[9], s[10], s[11])};
 #pragma unroll
-            for (int i = 4; i < kBlockN; i += 4) {
-                mx[0] = fmaxf(mx[0], s[i + 0]);
-                mx[1] = fmaxf(mx[1], s[i + 1]);
-                mx[2] = fmaxf(mx[2], s[i + 2]);
-                mx[3] = fmaxf(mx[3], s[i + 3]);
+            for (int i = 12; i + 8 <= kBlockN; i += 8) {
+                mx[0] = fmax3(mx[0], s[i + 0], s[i + 1]);
+                mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
+                mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
+                mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
             }
-            const float tile_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            const float m_new = fmaxf(m_run, tile_max * c2);
-            // correction factor; exp2(-inf) = 0 wipes the empty initial state,
-            // and a row with nothing visible yet keeps factor 1 (no -inf - -inf)
-            const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_run - m_new);
-            const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+            mx[0] = fmax3(mx[0], s[124], s[125]);
+            mx[1] = fmax3(mx[1], s[126], s[127]);
+            // scale > 0, so max(s) * c2 == max(s * c2)
+            const float m_cand = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2);
+            // move the reference only when the max grew past the threshold
+            // (always on the first visible tile: -inf + 64 = -inf < any finite max)
+            const bool move = m_cand > m_run + kRescaleThreshold;
+            const float alpha = move ? ex2_approx(m_run - m_cand) : 1.f;  // exp2(-inf) = 0 wipes the empty state
+            const bool any_move = __any_sync(0xffffffffu, move);
+            if (move) m_run = m_cand;
+            // a row with nothing visible yet keeps m = -inf and uses 0, so that its
+            // -inf scores give 0 rather than NaN
             uint32_t pk[kBlockN / 2];
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < kBlockN / 2; ++i) {
-                const float p0 = ex2_approx(fmaf(s[2 * i], c2, neg_m));
-                const float p1 = ex2_approx(fmaf(s[2 * i + 1], c2, neg_m));
-                rs[(2 * i) & 3] += p0;
-                rs[(2 * i + 1) & 3] += p1;
-                pk[i] = pack_bf16x2(p0, p1);
-            }
-            l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-            m_run = m_new;
-            if (j > 0) {
-                // O holds P_{j-1} V_{j-1} once that product has finished; rescale it
-                if (!fa_wait_warp(bar(L::kBarPV), (uint32_t)((j - 1) & 1), abort_flag, limit,
+            float sum_bf, sum_f32;
+            exp_row_tile(s, c2, (m_run == -INFINITY) ? 0.f : -m_run, pk, sum_bf, sum_f32);
+            l_run = l_run * alpha + sum_bf;
+            l32_run = l32_run * alpha + sum_f32;
+            if (j > 0 && any_move) {
+                // O must hold P_{j-1} V_{j-1} before it is rescaled
+                if (!fa_wait_warp(bar(L::kBarPVDone + (b ^ 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_flag, limit,
                                   kStatusSoftmaxWaitPV)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32_wait(t_lane + L::kColO + 32u * c, r);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32_wait(t_lane + L::kColO + 32u * c, r);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(t_lane + L::kColO + 32u * c, r);
-                    }
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st32(t_lane + L::kColO + 32u * c, r);
                 }
             }
-            const uint32_t pcol = t_lane + (b ? L::kColP1 : L::kColP0);
+            if (j >= 2) {
+                // P buffer b last fed P_{j-2} V_{j-2}: that product must have read it
+                if (!fa_wait_warp(bar(L::kBarPVDone + b), (uint32_t)(((j - 2) >> 1) & 1), abort_flag, limit,
+                                  kStatusSoftmaxWaitPV)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+            }
+            const uint32_t pcol = t_lane + L::col_p(b);
             tmem_st32(pcol, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
             tmem_st32(pcol + 32u, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
             tmem_st_wait();
@@ -399,9 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kBarPFull + b));
         }
-        if (ok)
-            ok = fa_wait_warp(bar(L::kBarPV), (uint32_t)((n_kv - 1) & 1), abort_flag, limit, kStatusSoftmaxWaitPV);
-        const uint32_t stage = sbase + L::kOffQ;  // Q is dead once the last S product has finished
+        if (ok) ok = fa_wait_warp(bar(L::kBarOFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
+        // Q is dead once the last S product has finished (the softmax read it): stage O there
+        const uint32_t stage = sbase + L::kOffQ;
         if (ok) {
             tc_fence_after_sync();
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -415,20 +473,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
                 const uint32_t chunk = stage + (uint32_t)(c >> 1) * kChunkBytes + (uint32_t)row * 128u;
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t u = (uint32_t)((c & 1) * 4 + t);  // 16-byte unit within the 128-byte row
-                    st_shared_v4(chunk + ((u ^ (uint32_t)(row & 7)) << 4), w[4 * t], w[4 * t + 1], w[4 * t + 2],
-                                 w[4 * t + 3]);
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const uint32_t u = (uint32_t)((c & 1) * 4 + u4);  // 16-byte unit within the 128-byte row
+                    st_shared_v4(chunk + ((u ^ (uint32_t)(row & 7)) << 4), w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2],
+                                 w[4 * u4 + 3]);
                 }
             }
             if (q_idx < p.N)
                 p.lse[(size_t)bh * (size_t)p.N + (size_t)q_idx] =
-                    l_run > 0.f ? (m_run + lg2_approx(l_run)) * kLn2 : -INFINITY;
+                    l32_run > 0.f ? (m_run + lg2_approx(l32_run)) * kLn2 : -INFINITY;
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         named_barrier_sync(1, 128);
-        if (warp == 2 && lane == 0 && *abort_flag == 0) {
+        if (warp == 4 && lane == 0 && *abort_flag == 0) {
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) tma_store_3d(&tm_o, stage + c * kChunkBytes, c * 64, qt * kBlockM, bh);
             bulk_commit_group();
