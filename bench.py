@@ -54,6 +54,27 @@ def row_flops(w, rows) -> float:
     return float(4.0 * w.d * n_vis.sum())
 
 
+def rank_workload(w, rank: int):
+    """Every rank solves its own problem: the same shapes, its own seed."""
+    return w.with_(seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time (a no-op for a single process)."""
+    if dist is None:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, steps: int, ms_total: float) -> float:
+    """Aggregate throughput: all ranks' FLOPs over the slowest rank's time."""
+    return world * flops_per_rank * steps / (ms_total * 1e-3) / 1e12
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -255,8 +276,7 @@ def main():
     dev = torch.device("cuda", local_rank)
     import online_softmax_04_gb300 as fa
 
-    # every rank solves its own problem: same shapes, its own seed
-    wr = w.with_(seed=w.seed + 1000 * rank)
+    wr = rank_workload(w, rank)
     q, k, v = wl.make_inputs(wr)
     dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
     o = torch.empty_like(dq)
@@ -301,10 +321,8 @@ def main():
             e1.record(stream)
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1)
+        ms = max_over_ranks(ms, dist, dev)
         if dist is not None:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
             dist.barrier()
         return ms
 
@@ -313,7 +331,7 @@ def main():
     clocks = clk.summary()
     ms_step = ms_total / args.steps
     flops = workload_flops(w)
-    value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, args.steps, ms_total)
 
     # end to end: pinned host buffers, copies inside the timed region
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
@@ -331,7 +349,7 @@ def main():
     for _ in range(3):
         e2e_step()
     ms_e2e = timed(e2e_step, args.steps)
-    e2e_value = world * flops * args.steps / (ms_e2e * 1e-3) / 1e12
+    e2e_value = whole_job_tflops(world, flops, args.steps, ms_e2e)
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 

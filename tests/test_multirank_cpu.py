@@ -1,0 +1,71 @@
+"""The N>1 host path of bench.py on a real two-rank gloo group (CPU only):
+distinct per-rank problems, max-over-ranks timing and the whole-job aggregate."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:  # the spawned ranks import this module afresh
+    sys.path.insert(0, ROOT)
+
+
+def free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def worker(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        from online_softmax_04_gb300 import workloads as wl
+
+        w = wl.WORKLOADS[wl.HEADLINE]
+        wr = bench.rank_workload(w, rank)
+        ms = bench.max_over_ranks(10.0 * (rank + 1), dist, "cpu")
+        value = bench.whole_job_tflops(world, bench.workload_flops(w), 7, ms)
+        out[rank] = (wr.seed, ms, value)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_gloo_aggregation():
+    world = 2
+    port = free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        ctx = mp.get_context("spawn")
+        procs = [ctx.Process(target=worker, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+        assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+        res = dict(out)
+    (s0, ms0, v0), (s1, ms1, v1) = res[0], res[1]
+    assert s0 != s1                       # independent problems per rank
+    assert ms0 == ms1 == 20.0             # both see the slowest rank
+    import bench
+    from online_softmax_04_gb300 import workloads as wl
+
+    f = bench.workload_flops(wl.WORKLOADS[wl.HEADLINE])
+    assert v0 == v1 == pytest.approx(2 * f * 7 / 0.020 / 1e12)
+
+
+def test_single_process_helpers():
+    import bench
+    from online_softmax_04_gb300 import workloads as wl
+
+    assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
+    w = wl.WORKLOADS["B4-H16-N4096-d128-causal"]
+    assert bench.workload_flops(w) == 4 * 4 * 16 * 4096 ** 2 * 128 / 2
+    assert bench.rank_workload(w, 0).seed == w.seed
