@@ -239,6 +239,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling captures)")
+    ap.add_argument("--splitkv", type=int, default=-1,
+                    help="use the split-KV entry point with this many splits (0 = automatic; default: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -283,8 +285,23 @@ def main():
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    n_splits = -1
+    if args.splitkv >= 0:
+        n_splits = args.splitkv or fa.fa_splitkv_auto_splits(w.B, w.H, w.N, w.d, w.causal)
+        ws_bytes = fa.fa_splitkv_workspace_bytes(w.B, w.H, w.N, w.d, n_splits)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def run_fwd():
+        if n_splits > 0:
+            fa.fa_fwd_splitkv(dq, dk, dv, o, lse, w.B, w.H, w.N, w.d, w.causal, w.scale, n_splits, workspace,
+                              ws_bytes, stream)
+        else:
+            fa.fa_fwd(dq, dk, dv, o, lse, w.B, w.H, w.N, w.d, w.causal, w.scale, stream)
+
+    launches_per_step = 2 if n_splits > 0 else 1
+
     def step():
-        fa.fa_fwd(dq, dk, dv, o, lse, w.B, w.H, w.N, w.d, w.causal, w.scale, stream)
+        run_fwd()
 
     fa.fa_clear_device_status()
     for _ in range(args.warmup):
@@ -342,7 +359,7 @@ def main():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        fa.fa_fwd(dq, dk, dv, o, lse, w.B, w.H, w.N, w.d, w.causal, w.scale, stream)
+        run_fwd()
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
@@ -361,8 +378,8 @@ def main():
         peak, peak_src = measured_peak()
         achieved = flops / (ms_step * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": recorded_traffic(w.name), "peak_source": peak_src,
-                    "kernel": KERNEL_NAME}
+                    "frac": achieved / peak, "traffic": recorded_traffic(w.name) if n_splits < 0 else None,
+                    "peak_source": peak_src, "kernel": KERNEL_NAME if n_splits < 0 else KERNEL_NAME + " + merge"}
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, q, k, v)
@@ -375,12 +392,13 @@ def main():
                        "l2": ("L2 flushed (512 MB write) before each individually timed step" if flush_l2 else
                               f"inputs larger than L2 ({io_bytes / 2**20:.0f} MiB of Q, K, V, O, LSE > 129 MB), "
                               "back-to-back steps, no flush"),
-                       "parallelism": f"independent problem per GPU x{world}"},
+                       "parallelism": f"independent problem per GPU x{world}",
+                       "entry_point": "fa_fwd" if n_splits < 0 else f"fa_fwd_splitkv (n_splits={n_splits})"},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ms_e2e / args.steps},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -59,7 +59,9 @@ enum {
     FA_ERR_ALIAS = -6,          /* o or lse overlaps q, k or v, or each other */
     FA_ERR_TENSOR_MAP = -7,     /* the driver rejected a TMA descriptor */
     FA_ERR_CUDA = -8,           /* a CUDA runtime call failed (launch, attribute, driver entry point) */
-    FA_ERR_DEVICE = -9          /* the current device is not an sm_103 GPU */
+    FA_ERR_DEVICE = -9,         /* the current device is not an sm_103 GPU */
+    FA_ERR_SPLITS = -10,        /* n_splits outside 0..64 */
+    FA_ERR_WORKSPACE = -11      /* split-KV workspace smaller than fa_splitkv_workspace_bytes() */
 };
 
 /*
@@ -81,6 +83,44 @@ enum {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_fwd_splitkv -- the same forward for problems with few query tiles.
+ *
+ * The key range of every query tile is cut into n_splits contiguous chunks
+ * of key tiles, each handled by its own CTA, so that small B*H*N still fills
+ * the GPU.  Each CTA leaves a partial row state -- reference max m, the sum of
+ * exponentials against it, and the unnormalised output -- in `workspace`; a
+ * merge kernel then combines the chunks with the associative rule of
+ * "5.2 CUDA Online Softmax", section 4.1 (m = max(m1, m2);
+ * d = d1 e^(m1 - m) + d2 e^(m2 - m), applied to the output as well) and writes
+ * o and lse exactly as fa_fwd does.
+ *
+ *   n_splits        : 1..64, or 0 to use fa_splitkv_auto_splits().  Chunks past
+ *                     a causal tile's diagonal are empty and weigh nothing.
+ *   workspace       : device memory owned by the caller, 16-byte aligned, at
+ *                     least fa_splitkv_workspace_bytes(B, H, N, d, n_splits)
+ *                     bytes, not overlapping any tensor; its contents on entry
+ *                     do not matter and are overwritten.
+ *   other arguments : as fa_fwd.
+ *
+ * Two kernels are enqueued on `stream`; calls sharing a workspace must not
+ * overlap on the GPU.  Returns FA_OK, an fa_fwd argument error, FA_ERR_SPLITS,
+ * FA_ERR_WORKSPACE, FA_ERR_ALIGNMENT or FA_ERR_NULL_POINTER for the workspace.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   int causal, float scale, int n_splits, void* workspace, size_t workspace_bytes,
+                   fa_stream_t stream);
+
+/* Workspace bytes fa_fwd_splitkv needs: n_splits * B*H*N * (d + 3) * 4; 0 for invalid arguments. */
+size_t fa_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
+
+/*
+ * A split count that fills about one wave of the current device (one CTA per
+ * SM): floor(SMs / (query tiles * B*H)), at most the number of key tiles and
+ * 64, at least 1.  Returns 1 when the plain fa_fwd already fills the GPU.
+ */
+int fa_splitkv_auto_splits(int B, int H, int N, int d, int causal);
 
 /* Human-readable name of an FA_* code; never NULL. */
 const char* fa_strerror(int code);

@@ -29,6 +29,8 @@ FA_ERR_ALIAS = -6
 FA_ERR_TENSOR_MAP = -7
 FA_ERR_CUDA = -8
 FA_ERR_DEVICE = -9
+FA_ERR_SPLITS = -10
+FA_ERR_WORKSPACE = -11
 
 _lock = threading.Lock()
 _lib = None
@@ -52,6 +54,12 @@ def lib() -> ctypes.CDLL:
             P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             L.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P]
             L.fa_fwd.restype = I
+            L.fa_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, ctypes.c_size_t, P]
+            L.fa_fwd_splitkv.restype = I
+            L.fa_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
+            L.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
+            L.fa_splitkv_auto_splits.argtypes = [I, I, I, I, I]
+            L.fa_splitkv_auto_splits.restype = I
             L.fa_strerror.argtypes = [I]
             L.fa_strerror.restype = ctypes.c_char_p
             L.fa_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
@@ -116,6 +124,43 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, B, H, N, d, causal, (1.0 / math.sqrt(d)) if scale is None else scale, stream)
+    return o, lse
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B: int, H: int, N: int, d: int, causal: bool, scale: float, n_splits: int,
+                   workspace, workspace_bytes: int, stream=None) -> None:
+    """Enqueue the split-KV forward and its merge; raises FaError on a nonzero C return code."""
+    rc = lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
+                              1 if causal else 0, float(scale), int(n_splits), _ptr(workspace), int(workspace_bytes),
+                              _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+
+
+def fa_splitkv_workspace_bytes(B: int, H: int, N: int, d: int, n_splits: int) -> int:
+    return int(lib().fa_splitkv_workspace_bytes(int(B), int(H), int(N), int(d), int(n_splits)))
+
+
+def fa_splitkv_auto_splits(B: int, H: int, N: int, d: int, causal: bool) -> int:
+    return int(lib().fa_splitkv_auto_splits(int(B), int(H), int(N), int(d), 1 if causal else 0))
+
+
+def attention_splitkv(q, k, v, causal: bool = False, scale: float | None = None, n_splits: int = 0, workspace=None,
+                      stream=None):
+    """Split-KV forward; allocates the workspace with torch when none is given."""
+    import torch
+
+    B, H, N, d = q.shape
+    if n_splits == 0:
+        n_splits = fa_splitkv_auto_splits(B, H, N, d, causal)
+    need = fa_splitkv_workspace_bytes(B, H, N, d, n_splits)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else need
+    fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, causal, (1.0 / math.sqrt(d)) if scale is None else scale, n_splits,
+                   workspace, nbytes, stream)
     return o, lse
 
 

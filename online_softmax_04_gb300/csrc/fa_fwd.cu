@@ -71,26 +71,36 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-template <int D, int NK, int NV>
+template <int D, int NK, int NV, bool kSplit>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
            const fa::FaParams& p, int BH, cudaStream_t stream) {
     using L = fa::FaSmem<D, NK, NV>;
-    auto kern = fa::fa_fwd_sm103<D, NK, NV>;
+    auto kern = fa::fa_fwd_sm103<D, NK, NV, kSplit>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
         return FA_ERR_CUDA;
-    // one CTA per 128-row query tile; blockIdx.x runs from the last (longest
-    // causal) tile down, so the heaviest CTAs are scheduled first
-    dim3 grid((unsigned)p.n_tiles, (unsigned)BH, 1);
+    // one CTA per 128-row query tile (and per key split); blockIdx.x runs from
+    // the last (longest causal) tile down, so the heaviest CTAs start first
+    dim3 grid((unsigned)p.n_tiles, (unsigned)BH, kSplit ? (unsigned)p.n_splits : 1u);
     kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-}  // namespace
+template <bool kSplit>
+int launch_d(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+             const fa::FaParams& p, int BH, cudaStream_t s) {
+    if (d == 64) return launch<64, 6, 6, kSplit>(tq, tk, tv, to, p, BH, s);
+    return launch<128, 3, 3, kSplit>(tq, tk, tv, to, p, BH, s);
+}
 
-extern "C" {
+struct Prepared {
+    CUtensorMap tq, tk, tv, to;
+    fa::FaParams p;
+    int BH;
+};
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
-           float scale, fa_stream_t stream) {
+// Host-side argument validation shared by the entry points (no CUDA calls).
+int validate(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             float scale) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
     if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
     if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
@@ -107,27 +117,131 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         overlaps(lse, lse_bytes, k, tensor_bytes) || overlaps(lse, lse_bytes, v, tensor_bytes) ||
         overlaps(lse, lse_bytes, o, tensor_bytes))
         return FA_ERR_ALIAS;
+    return FA_OK;
+}
+
+// The device check and the TMA descriptors, after validate() passed.
+int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
+            float scale, Prepared* out) {
+    const long long BH = (long long)B * (long long)H;
     const int dev_rc = check_device();
     if (dev_rc != FA_OK) return dev_rc;
-
-    CUtensorMap tq, tk, tv, to;
-    if (!encode_bhnd(&tq, q, d, N, (int)BH) || !encode_bhnd(&tk, k, d, N, (int)BH) ||
-        !encode_bhnd(&tv, v, d, N, (int)BH) || !encode_bhnd(&to, o, d, N, (int)BH))
+    if (!encode_bhnd(&out->tq, q, d, N, (int)BH) || !encode_bhnd(&out->tk, k, d, N, (int)BH) ||
+        !encode_bhnd(&out->tv, v, d, N, (int)BH) || !encode_bhnd(&out->to, o, d, N, (int)BH))
         return FA_ERR_TENSOR_MAP;
-
-    fa::FaParams p;
+    fa::FaParams& p = out->p;
+    p = fa::FaParams{};
     p.lse = lse;
     p.N = N;
     p.n_tiles = (N + fa::kBlockN - 1) / fa::kBlockN;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = scale * 1.44269504088896340736f;
+    p.n_splits = 1;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         p.watchdog_ns = g_watchdog_ns;
     }
+    out->BH = (int)BH;
+    return FA_OK;
+}
+
+constexpr int kMaxSplits = 64;
+
+size_t splitkv_bytes(long long BH, long long N, int d, int n_splits) {
+    return (size_t)n_splits * (size_t)BH * (size_t)N * (size_t)(d + 3) * sizeof(float);
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
+           float scale, fa_stream_t stream) {
+    int rc = validate(q, k, v, o, lse, B, H, N, d, scale);
+    if (rc != FA_OK) return rc;
+    Prepared pr;
+    rc = prepare(q, k, v, o, lse, B, H, N, d, causal, scale, &pr);
+    if (rc != FA_OK) return rc;
+    return launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.to, pr.p, pr.BH, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fa_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || n_splits < 1 || n_splits > kMaxSplits) return 0;
+    return splitkv_bytes((long long)B * H, N, d, n_splits);
+}
+
+int fa_splitkv_auto_splits(int B, int H, int N, int d, int causal) {
+    (void)d;
+    (void)causal;
+    if (B < 1 || H < 1 || N < 1) return 1;
+    const long long tiles = (N + fa::kBlockN - 1) / fa::kBlockN;
+    const long long ctas = tiles * (long long)B * H;
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    if (ctas >= sms) return 1;
+    long long s = sms / ctas;  // fill at most one wave of one-CTA-per-SM blocks
+    if (s > tiles) s = tiles;
+    if (s > kMaxSplits) s = kMaxSplits;
+    return s < 1 ? 1 : (int)s;
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   int causal, float scale, int n_splits, void* workspace, size_t workspace_bytes,
+                   fa_stream_t stream) {
+    int rc = validate(q, k, v, o, lse, B, H, N, d, scale);
+    if (rc != FA_OK) return rc;
+    if (n_splits < 0 || n_splits > kMaxSplits) return FA_ERR_SPLITS;
+    if (!workspace) return FA_ERR_NULL_POINTER;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return FA_ERR_ALIGNMENT;
+    const long long BH = (long long)B * (long long)H;
+    // the automatic count needs the device; size checks use the worst case first
+    const size_t tensor_bytes = (size_t)BH * (size_t)N * (size_t)d * 2u;
+    const size_t lse_bytes = (size_t)BH * (size_t)N * 4u;
+    if (n_splits > 0) {
+        const size_t need = splitkv_bytes(BH, N, d, n_splits);
+        if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+        if (overlaps(workspace, need, q, tensor_bytes) || overlaps(workspace, need, k, tensor_bytes) ||
+            overlaps(workspace, need, v, tensor_bytes) || overlaps(workspace, need, o, tensor_bytes) ||
+            overlaps(workspace, need, lse, lse_bytes))
+            return FA_ERR_ALIAS;
+    }
+    Prepared pr;
+    rc = prepare(q, k, v, o, lse, B, H, N, d, causal, scale, &pr);
+    if (rc != FA_OK) return rc;
+    if (n_splits == 0) {
+        n_splits = fa_splitkv_auto_splits(B, H, N, d, causal);
+        const size_t need = splitkv_bytes(BH, N, d, n_splits);
+        if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+        if (overlaps(workspace, need, q, tensor_bytes) || overlaps(workspace, need, k, tensor_bytes) ||
+            overlaps(workspace, need, v, tensor_bytes) || overlaps(workspace, need, o, tensor_bytes) ||
+            overlaps(workspace, need, lse, lse_bytes))
+            return FA_ERR_ALIAS;
+    }
+    const long long rows = (long long)pr.BH * N;
+    float* ws = static_cast<float*>(workspace);
+    pr.p.n_splits = n_splits;
+    pr.p.ws_o = ws;
+    pr.p.ws_m = ws + (size_t)n_splits * rows * d;
+    pr.p.ws_lbf = pr.p.ws_m + (size_t)n_splits * rows;
+    pr.p.ws_l32 = pr.p.ws_lbf + (size_t)n_splits * rows;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (d == 64) return launch<64, 6, 6>(tq, tk, tv, to, p, (int)BH, s);
-    return launch<128, 3, 3>(tq, tk, tv, to, p, (int)BH, s);
+    const int lrc = launch_d<true>(d, pr.tq, pr.tk, pr.tv, pr.to, pr.p, pr.BH, s);
+    if (lrc != FA_OK) return lrc;
+    const unsigned blocks = (unsigned)((rows + 7) / 8);  // 8 warps per block, one row per warp
+    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+    if (d == 64)
+        fa::fa_splitkv_merge<64><<<blocks, 256, 0, s>>>(pr.p.ws_o, pr.p.ws_m, pr.p.ws_lbf, pr.p.ws_l32, ob, lse, rows,
+                                                        n_splits);
+    else
+        fa::fa_splitkv_merge<128><<<blocks, 256, 0, s>>>(pr.p.ws_o, pr.p.ws_m, pr.p.ws_lbf, pr.p.ws_l32, ob, lse,
+                                                         rows, n_splits);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 const char* fa_strerror(int code) {
@@ -142,6 +256,8 @@ const char* fa_strerror(int code) {
         case FA_ERR_TENSOR_MAP: return "the driver rejected a TMA tensor map";
         case FA_ERR_CUDA: return "a CUDA runtime call failed";
         case FA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+        case FA_ERR_SPLITS: return "n_splits must be 0 (automatic) or 1..64";
+        case FA_ERR_WORKSPACE: return "the split-KV workspace is smaller than fa_splitkv_workspace_bytes()";
         default: return "unknown error code";
     }
 }

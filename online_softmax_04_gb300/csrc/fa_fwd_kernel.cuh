@@ -50,6 +50,8 @@
 // and MMAs drain, frees TMEM and exits.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -89,6 +91,12 @@ struct FaParams {
     int causal;
     float scale_log2;  // scale * log2(e)
     unsigned long long watchdog_ns;
+    // split-KV partial states (kSplit kernels only): [n_splits][B*H][N] rows
+    int n_splits;
+    float* ws_o;    // unnormalised O, fp32 [rows][d]
+    float* ws_m;    // reference max, base-2 units
+    float* ws_lbf;  // sum of the bf16-rounded exponentials
+    float* ws_l32;  // fp32 sum of the exponentials
 };
 
 template <int D, int NK, int NV>
@@ -189,7 +197,11 @@ __device__ __forceinline__ void exp_row_tile(const float (&s)[kBlockN], float c2
     sum_f32 = (e0 + o0) + (e1 + o1);
 }
 
-template <int D, int NK, int NV>
+// kSplit: the CTA covers only the key tiles of split blockIdx.z and writes the
+// partial row state (m, both sums, unnormalised O) instead of O and LSE; a
+// merge kernel combines the splits ("5.2 CUDA Online Softmax", section 4.1:
+// the (m, d) merge is associative, so partial results combine in any order).
+template <int D, int NK, int NV, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -206,7 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = (int)(threadIdx.x & 31);
     const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest causal rows first
     const int bh = (int)blockIdx.y;
-    const int n_kv = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;
+    const int n_all = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;  // key tiles this query tile sees
+    int j0 = 0, n_kv = n_all;  // this CTA's key tiles: j0 .. j0 + n_kv - 1
+    if constexpr (kSplit) {
+        const int chunk = (n_all + p.n_splits - 1) / p.n_splits;
+        j0 = (int)blockIdx.z * chunk;
+        n_kv = max(0, min(n_all - j0, chunk));
+    }
     const uint64_t limit = p.watchdog_ns;
 
     if (warp == 0 && lane == 0) {
@@ -251,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // TMA producer: Q once; K_0, K_1; then V_j and K_{j+2}, the order in
         // which the two MMA issuers consume them.
         // ------------------------------------------------------------------
-        if (lane == 0) {
+        if (lane == 0 && n_kv > 0) {
             mbar_arrive_expect_tx(bar(L::kBarQ), L::kTileBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
@@ -265,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kOffK + s * L::kTileBytes + c * kChunkBytes, &tm_k, bar(L::kBarKFull + s),
-                                c * 64, j * kBlockN, bh);
+                                c * 64, (j0 + j) * kBlockN, bh);
                 ++nk;
                 return true;
             };
@@ -277,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kOffV + s * L::kTileBytes + c * kChunkBytes, &tm_v, bar(L::kBarVFull + s),
-                                c * 64, j * kBlockN, bh);
+                                c * 64, (j0 + j) * kBlockN, bh);
                 ++nv;
                 return true;
             };
@@ -305,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
             const uint32_t qa = sbase + L::kOffQ;
-            bool ok = fa_wait(bar(L::kBarQ), 0, abort_flag, limit, kStatusMmaWaitQ);
+            bool ok = n_kv > 0 && fa_wait(bar(L::kBarQ), 0, abort_flag, limit, kStatusMmaWaitQ);
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int b = j & 1;
                 const int ks = j % NK;
@@ -391,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kBarSFree + b));
             // mask keys past the diagonal (causal) and past the end of the sequence
-            int lim = p.N - 1 - j * kBlockN;
-            if (p.causal && j == qt) lim = min(lim, row);
+            int lim = p.N - 1 - (j0 + j) * kBlockN;
+            if (p.causal && j0 + j == qt) lim = min(lim, row);
             if (lim < kBlockN - 1) {
 #pragma unroll
                 for (int i = 0; i < kBlockN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
@@ -457,7 +475,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kBarPFull + b));
         }
-        if (ok) ok = fa_wait_warp(bar(L::kBarOFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
+        if (ok && n_kv > 0) ok = fa_wait_warp(bar(L::kBarOFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
+        if constexpr (kSplit) {
+            // partial state of this split: unnormalised O and (m, sums) per row.
+            // The TMEM loads are warp-collective, so every lane runs them and
+            // only rows inside the sequence store.
+            const bool valid = q_idx < p.N;
+            const size_t r = ((size_t)blockIdx.z * gridDim.y + (size_t)bh) * (size_t)p.N + (size_t)q_idx;
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + r * D);
+            if (ok && n_kv > 0) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32_wait(t_lane + L::kColO + 32u * c, v);
+                    if (valid) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            dst[c * 8 + u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                                         __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+                    }
+                }
+            } else if (ok && valid) {
+#pragma unroll
+                for (int u = 0; u < D / 4; ++u) dst[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (ok && valid) {
+                p.ws_m[r] = m_run;
+                p.ws_lbf[r] = l_run;
+                p.ws_l32[r] = l32_run;
+            }
+            tc_fence_before_sync();
+        } else {
         // Q is dead once the last S product has finished (the softmax read it): stage O there
         const uint32_t stage = sbase + L::kOffQ;
         if (ok) {
@@ -492,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit_group();
             bulk_wait_group_all();
         }
+        }  // kSplit
         __syncwarp();
     }
 
@@ -501,6 +551,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Split-KV merge: one warp per query row combines the partial states of all
+// splits with the associative rule m = max_s m_s, w_s = 2^(m_s - m),
+// l = sum_s w_s l_s, O = sum_s w_s O_s / l ("5.2 CUDA Online Softmax",
+// section 4.1), then writes O (bf16) and LSE.  Splits that saw no key carry
+// m = -inf and weigh nothing.
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_splitkv_merge(const float* __restrict__ ws_o, const float* __restrict__ ws_m, const float* __restrict__ ws_lbf,
+                     const float* __restrict__ ws_l32, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                     long long rows, int n_splits) {
+    const long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    float m = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) m = fmaxf(m, ws_m[(size_t)s * rows + row]);
+    float l = 0.f, l32 = 0.f, acc[D / 32];
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) acc[c] = 0.f;
+    for (int s = 0; s < n_splits; ++s) {
+        const size_t r = (size_t)s * rows + row;
+        const float ms = ws_m[r];
+        const float w = (ms == -INFINITY) ? 0.f : ex2_approx(ms - m);
+        l += w * ws_lbf[r];
+        l32 += w * ws_l32[r];
+        const float* src = ws_o + r * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) acc[c] += w * src[c * 32 + lane];
+    }
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* dst = o + (size_t)row * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) dst[c * 32 + lane] = __float2bfloat16_rn(acc[c] * inv_l);
+    if (lane == 0) lse[row] = l32 > 0.f ? (m + lg2_approx(l32)) * kLn2 : -INFINITY;
 }
 
 // One CTA waits on a barrier nothing arrives on; the watchdog must end the

@@ -90,3 +90,33 @@ def test_product_does_not_import_the_oracle():
     for name in os.listdir(os.path.join(pkg, "csrc")):
         src = open(os.path.join(pkg, "csrc", name)).read()
         assert "oracle" not in src, name
+
+
+def test_splitkv_host_validation(fa):
+    L = fa.lib()
+    W = FAKE + (5 << 30)
+
+    def sk(n_splits=2, ws=W, wsb=1 << 30, **kw):
+        a = dict(q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), o=FAKE + (3 << 30), lse=FAKE + (4 << 30), B=1, H=1,
+                 N=128, d=64, causal=0, scale=0.125)
+        a.update(kw)
+        return L.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                                a["causal"], a["scale"], n_splits, ws, wsb, 0)
+
+    assert sk(n_splits=65) == fa.FA_ERR_SPLITS
+    assert sk(n_splits=-1) == fa.FA_ERR_SPLITS
+    assert sk(ws=0) == fa.FA_ERR_NULL_POINTER
+    assert sk(ws=W + 4) == fa.FA_ERR_ALIGNMENT
+    assert sk(wsb=10) == fa.FA_ERR_WORKSPACE
+    assert sk(ws=FAKE + 16) == fa.FA_ERR_ALIAS
+    assert sk(d=96) == fa.FA_ERR_HEAD_DIM  # the fa_fwd checks come first
+
+
+def test_splitkv_workspace_formula(fa):
+    assert fa.fa_splitkv_workspace_bytes(1, 1, 4096, 64, 4) == 4 * 4096 * (64 + 3) * 4
+    assert fa.fa_splitkv_workspace_bytes(2, 3, 100, 128, 7) == 7 * 6 * 100 * 131 * 4
+    assert fa.fa_splitkv_workspace_bytes(1, 1, 128, 96, 2) == 0
+    assert fa.fa_splitkv_workspace_bytes(1, 1, 128, 64, 65) == 0
+    # automatic count: never more than the key tiles, 1 once the plain grid fills the GPU
+    assert 1 <= fa.fa_splitkv_auto_splits(1, 1, 256, 64, 0) <= 2
+    assert fa.fa_splitkv_auto_splits(1, 32, 16384, 128, 1) == 1
