@@ -61,8 +61,12 @@ enum {
     FA_ERR_CUDA = -8,           /* a CUDA runtime call failed (launch, attribute, driver entry point) */
     FA_ERR_DEVICE = -9,         /* the current device is not an sm_103 GPU */
     FA_ERR_SPLITS = -10,        /* n_splits outside 0..64 */
-    FA_ERR_WORKSPACE = -11      /* split-KV workspace smaller than fa_splitkv_workspace_bytes() */
+    FA_ERR_WORKSPACE = -11,     /* split-KV workspace smaller than fa_splitkv_workspace_bytes() */
+    FA_ERR_SCRATCH_LIMIT = -12  /* fa_fwd_splitkv_noalloc: partial states exceed FA_NOALLOC_SCRATCH_BYTES */
 };
+
+/* Size of the library's static split-KV scratch used by fa_fwd_splitkv_noalloc (32 MiB). */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /*
  * fa_fwd -- fused attention forward.
@@ -111,6 +115,36 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                    int causal, float scale, int n_splits, void* workspace, size_t workspace_bytes,
                    fa_stream_t stream);
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv without a caller workspace and
+ * without allocating anything.  (An addition of this library; the pages have
+ * no counterpart.)
+ *
+ * For callers that cannot allocate device memory when they run attention:
+ * code whose device memory is owned by a host framework or an engine with a
+ * fixed budget, or a latency-critical path that must not pay for cudaMalloc
+ * and the device-wide synchronisation it may imply.  Instead of a workspace,
+ * the partial states live in one static device array inside this library,
+ * FA_NOALLOC_SCRATCH_BYTES (32 MiB) large, which every GPU that loads the
+ * library keeps until the process exits.
+ *
+ *   arguments       : as fa_fwd_splitkv, minus workspace and workspace_bytes.
+ *   n_splits        : 1..64, or 0 for the automatic count, lowered as needed
+ *                     until n_splits * B*H*N * (d + 3) * 4 bytes fit.
+ *
+ * Returns FA_ERR_SCRATCH_LIMIT, enqueueing nothing, when the partial states
+ * do not fit in FA_NOALLOC_SCRATCH_BYTES; other codes as fa_fwd_splitkv.
+ *
+ * The first call on a device looks up the array's device address (a
+ * cudaGetSymbolAddress with that device current) and caches it; make that
+ * first call before any stream capture.  The array is shared by every call
+ * and keeps whatever the last call left in it, none of which is read by the
+ * next call.  Calls that may run at the same time on the GPU (two streams,
+ * two host threads) race on it and must be serialised by the caller.
+ */
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                           int d, int causal, float scale, int n_splits, fa_stream_t stream);
 
 /* Workspace bytes fa_fwd_splitkv needs: n_splits * B*H*N * (d + 3) * 4; 0 for invalid arguments. */
 size_t fa_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);

@@ -31,6 +31,8 @@ FA_ERR_CUDA = -8
 FA_ERR_DEVICE = -9
 FA_ERR_SPLITS = -10
 FA_ERR_WORKSPACE = -11
+FA_ERR_SCRATCH_LIMIT = -12
+FA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -56,6 +58,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd.restype = I
             L.fa_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, ctypes.c_size_t, P]
             L.fa_fwd_splitkv.restype = I
+            L.fa_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P]
+            L.fa_fwd_splitkv_noalloc.restype = I
             L.fa_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
             L.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
             L.fa_splitkv_auto_splits.argtypes = [I, I, I, I, I]
@@ -133,6 +137,20 @@ def fa_fwd_splitkv(q, k, v, o, lse, B: int, H: int, N: int, d: int, causal: bool
     rc = lib().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
                               1 if causal else 0, float(scale), int(n_splits), _ptr(workspace), int(workspace_bytes),
                               _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B: int, H: int, N: int, d: int, causal: bool, scale: float,
+                           n_splits: int = 0, stream=None) -> None:
+    """Split-KV forward for callers that cannot allocate device memory when they
+    run attention: its partial states go to a static 32 MiB array inside the
+    library, shared by every call.  Calls that may overlap on the GPU must be
+    serialised by the caller; the first call on a device should come before any
+    stream capture.  Raises FaError (FA_ERR_SCRATCH_LIMIT when the problem does
+    not fit)."""
+    rc = lib().fa_fwd_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
+                                      1 if causal else 0, float(scale), int(n_splits), _stream(stream))
     if rc != FA_OK:
         raise FaError(rc, fa_strerror(rc))
 

@@ -158,6 +158,31 @@ int sm_count() {
     return n;
 }
 
+// ----------------------------------------------------------------------------
+// Static scratch for fa_fwd_splitkv_noalloc.  It lives in the module image, so
+// every device that loads this library holds FA_NOALLOC_SCRATCH_BYTES of it
+// until the process exits.  Host code only ever names it to ask the runtime
+// for its device address (once per device); the kernels get that address.
+// ----------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+void* g_noalloc_addr[kMaxDevices];  // device address of the scratch, per device (nullptr: not looked up yet)
+
+// Device address of the scratch on the current device, looked up on first use.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_fa_noalloc_scratch) != cudaSuccess || !ptr) return FA_ERR_CUDA;
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -244,6 +269,50 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                           int d, int causal, float scale, int n_splits, fa_stream_t stream) {
+    int rc = validate(q, k, v, o, lse, B, H, N, d, scale);
+    if (rc != FA_OK) return rc;
+    if (n_splits < 0 || n_splits > kMaxSplits) return FA_ERR_SPLITS;
+    const long long BH = (long long)B * (long long)H;
+    if (n_splits > 0 && splitkv_bytes(BH, N, d, n_splits) > (size_t)FA_NOALLOC_SCRATCH_BYTES)
+        return FA_ERR_SCRATCH_LIMIT;
+    Prepared pr;
+    rc = prepare(q, k, v, o, lse, B, H, N, d, causal, scale, &pr);
+    if (rc != FA_OK) return rc;
+    if (n_splits == 0) {
+        // the automatic count, reduced until the partial states fit the scratch
+        n_splits = fa_splitkv_auto_splits(B, H, N, d, causal);
+        while (n_splits > 1 && splitkv_bytes(BH, N, d, n_splits) > (size_t)FA_NOALLOC_SCRATCH_BYTES) --n_splits;
+        if (splitkv_bytes(BH, N, d, n_splits) > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+    }
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != FA_OK) return rc;
+    // Every partial state the merge reads is written by the split kernel of the
+    // same call (empty chunks write m = -inf and zeros), so whatever an earlier
+    // call left in the scratch never needs clearing.
+    const long long rows = BH * N;
+    float* ws = static_cast<float*>(scratch);
+    pr.p.n_splits = n_splits;
+    pr.p.ws_o = ws;
+    pr.p.ws_m = ws + (size_t)n_splits * rows * d;
+    pr.p.ws_lbf = pr.p.ws_m + (size_t)n_splits * rows;
+    pr.p.ws_l32 = pr.p.ws_lbf + (size_t)n_splits * rows;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int lrc = launch_d<true>(d, pr.tq, pr.tk, pr.tv, pr.to, pr.p, pr.BH, s);
+    if (lrc != FA_OK) return lrc;
+    const unsigned blocks = (unsigned)((rows + 7) / 8);
+    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+    if (d == 64)
+        fa::fa_splitkv_merge<64><<<blocks, 256, 0, s>>>(pr.p.ws_o, pr.p.ws_m, pr.p.ws_lbf, pr.p.ws_l32, ob, lse, rows,
+                                                        n_splits);
+    else
+        fa::fa_splitkv_merge<128><<<blocks, 256, 0, s>>>(pr.p.ws_o, pr.p.ws_m, pr.p.ws_lbf, pr.p.ws_l32, ob, lse,
+                                                         rows, n_splits);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 const char* fa_strerror(int code) {
     switch (code) {
         case FA_OK: return "ok";
@@ -258,6 +327,8 @@ const char* fa_strerror(int code) {
         case FA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
         case FA_ERR_SPLITS: return "n_splits must be 0 (automatic) or 1..64";
         case FA_ERR_WORKSPACE: return "the split-KV workspace is smaller than fa_splitkv_workspace_bytes()";
+        case FA_ERR_SCRATCH_LIMIT:
+            return "the partial states need more than FA_NOALLOC_SCRATCH_BYTES; call fa_fwd_splitkv with a workspace";
         default: return "unknown error code";
     }
 }
