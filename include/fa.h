@@ -53,7 +53,7 @@ enum {
     FA_OK = 0,
     FA_ERR_NULL_POINTER = -1,   /* q, k, v, o or lse is NULL */
     FA_ERR_HEAD_DIM = -2,       /* d is not 64 or 128 */
-    FA_ERR_SHAPE = -3,          /* B, H or N < 1, or B*H > 65535 */
+    FA_ERR_SHAPE = -3,          /* B, H or N < 1, B*H > 65535, or B*H*ceil(N/128) >= 2^31 */
     FA_ERR_ALIGNMENT = -4,      /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
     FA_ERR_SCALE = -5,          /* scale not finite or not > 0 */
     FA_ERR_ALIAS = -6,          /* o or lse overlaps q, k or v, or each other */
@@ -84,6 +84,11 @@ enum {
  *
  * Inputs are not modified.  o and lse must not overlap q, k, v or each other.
  * Returns FA_OK once the kernel is enqueued.
+ *
+ * The kernel is persistent (at most one CTA per SM) and takes its query tiles
+ * from a work counter in the library's static device memory; each call uses
+ * the next of 1024 counters in turn, so calls may run concurrently on several
+ * streams as long as fewer than 1024 of them are in flight at once.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            int causal, float scale, fa_stream_t stream);

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -71,29 +72,44 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+int sm_count();
+
+// kSplit: one CTA per (query tile, head, key split).  Otherwise a persistent
+// grid of at most one CTA per SM walks the work items (see fa::TileSeq).
 template <int D, int NK, int NV, bool kSplit>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-           const fa::FaParams& p, int BH, cudaStream_t stream) {
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, fa::FaParams p, int BH,
+           cudaStream_t stream) {
     using L = fa::FaSmem<D, NK, NV>;
-    auto kern = fa::fa_fwd_sm103<D, NK, NV, kSplit>;
+    constexpr bool kPersistent = !kSplit;
+    auto kern = fa::fa_fwd_sm103<D, NK, NV, kSplit, kPersistent>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
         return FA_ERR_CUDA;
-    // one CTA per 128-row query tile (and per key split); blockIdx.x runs from
-    // the last (longest causal) tile down, so the heaviest CTAs start first
-    dim3 grid((unsigned)p.n_tiles, (unsigned)BH, kSplit ? (unsigned)p.n_splits : 1u);
-    kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, to, p);
+    dim3 grid;
+    if constexpr (kSplit) {
+        // blockIdx.x runs from the last (longest causal) tile down: heaviest first
+        grid = dim3((unsigned)p.n_tiles, (unsigned)BH, (unsigned)p.n_splits);
+    } else {
+        const int sms = sm_count() > 0 ? sm_count() : 148;
+        const long long pairs = fa::persistent_pairs(p);
+        const long long tiles = (long long)BH * p.n_tiles;
+        const long long ctas = tiles < sms ? tiles : sms;
+        grid = dim3((unsigned)ctas, 1, 1);
+        // about the last 15% of the pairs go to the dynamic tail
+        p.static_rounds = (int)((pairs * 85) / (100 * ctas));
+    }
+    kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 template <bool kSplit>
-int launch_d(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-             const fa::FaParams& p, int BH, cudaStream_t s) {
-    if (d == 64) return launch<64, 6, 6, kSplit>(tq, tk, tv, to, p, BH, s);
-    return launch<128, 3, 3, kSplit>(tq, tk, tv, to, p, BH, s);
+int launch_d(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::FaParams& p,
+             int BH, cudaStream_t s) {
+    if (d == 64) return launch<64, 6, 6, kSplit>(tq, tk, tv, p, BH, s);
+    return launch<128, 2, 3, kSplit>(tq, tk, tv, p, BH, s);
 }
 
 struct Prepared {
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     fa::FaParams p;
     int BH;
 };
@@ -106,6 +122,8 @@ int validate(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
     const long long BH = (long long)B * (long long)H;
     if (BH > 65535) return FA_ERR_SHAPE;
+    // the persistent schedule numbers the (head, query tile) pairs in 32 bits
+    if (BH * (((long long)N + fa::kBlockN - 1) / fa::kBlockN) >= (1ll << 31)) return FA_ERR_SHAPE;
     auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
     if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
         return FA_ERR_ALIGNMENT;
@@ -127,11 +145,13 @@ int prepare(const void* q, const void* k, const void* v, void* o, float* lse, in
     const int dev_rc = check_device();
     if (dev_rc != FA_OK) return dev_rc;
     if (!encode_bhnd(&out->tq, q, d, N, (int)BH) || !encode_bhnd(&out->tk, k, d, N, (int)BH) ||
-        !encode_bhnd(&out->tv, v, d, N, (int)BH) || !encode_bhnd(&out->to, o, d, N, (int)BH))
+        !encode_bhnd(&out->tv, v, d, N, (int)BH))
         return FA_ERR_TENSOR_MAP;
     fa::FaParams& p = out->p;
     p = fa::FaParams{};
+    p.o = o;
     p.lse = lse;
+    p.BH = (int)BH;
     p.N = N;
     p.n_tiles = (N + fa::kBlockN - 1) / fa::kBlockN;
     p.causal = causal ? 1 : 0;
@@ -183,6 +203,35 @@ int noalloc_scratch(void** out) {
     return FA_OK;
 }
 
+// ----------------------------------------------------------------------------
+// Work-queue counters of the persistent kernel: {next item, CTAs finished} per
+// slot, zero at load time and left at zero by the last CTA of every launch.
+// Each fa_fwd call takes the next slot round-robin, so that calls running at
+// the same time on different streams do not share a counter (unless more than
+// kQueueSlots - 1 launches are in flight at once).
+// ----------------------------------------------------------------------------
+constexpr unsigned kQueueSlots = 1024;
+static __device__ unsigned int g_fa_queue[2 * kQueueSlots];
+
+unsigned int* g_queue_addr[kMaxDevices];
+std::atomic<unsigned> g_queue_seq{0};
+
+int queue_slot(unsigned int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_queue_addr[dev]) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_fa_queue) != cudaSuccess || !ptr) return FA_ERR_CUDA;
+            g_queue_addr[dev] = static_cast<unsigned int*>(ptr);
+        }
+    }
+    *out = g_queue_addr[dev] + 2u * (g_queue_seq.fetch_add(1u) % kQueueSlots);
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -194,7 +243,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     Prepared pr;
     rc = prepare(q, k, v, o, lse, B, H, N, d, causal, scale, &pr);
     if (rc != FA_OK) return rc;
-    return launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.to, pr.p, pr.BH, reinterpret_cast<cudaStream_t>(stream));
+    rc = queue_slot(&pr.p.queue);
+    if (rc != FA_OK) return rc;
+    return launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t fa_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits) {
@@ -256,7 +307,7 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
     pr.p.ws_lbf = pr.p.ws_m + (size_t)n_splits * rows;
     pr.p.ws_l32 = pr.p.ws_lbf + (size_t)n_splits * rows;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int lrc = launch_d<true>(d, pr.tq, pr.tk, pr.tv, pr.to, pr.p, pr.BH, s);
+    const int lrc = launch_d<true>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, s);
     if (lrc != FA_OK) return lrc;
     const unsigned blocks = (unsigned)((rows + 7) / 8);  // 8 warps per block, one row per warp
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
@@ -300,7 +351,7 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
     pr.p.ws_lbf = pr.p.ws_m + (size_t)n_splits * rows;
     pr.p.ws_l32 = pr.p.ws_lbf + (size_t)n_splits * rows;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int lrc = launch_d<true>(d, pr.tq, pr.tk, pr.tv, pr.to, pr.p, pr.BH, s);
+    const int lrc = launch_d<true>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, s);
     if (lrc != FA_OK) return lrc;
     const unsigned blocks = (unsigned)((rows + 7) / 8);
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);

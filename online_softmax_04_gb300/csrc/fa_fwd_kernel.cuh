@@ -1,7 +1,7 @@
 // fa_fwd_kernel.cuh -- fused attention forward for sm_103a (GB300).
 //
-// One CTA owns one 128-row query tile of one (batch, head) and streams the
-// key/value tiles past it ("Online Softmax: Tiling Across a Reduction", loop
+// A 128-row query tile of one (batch, head) stays resident while the key/value
+// tiles stream past it ("Online Softmax: Tiling Across a Reduction", loop
 // order: query blocks outer and resident, key/value blocks inner).  Per key
 // tile j each query row updates its state with one correction factor
 // ("Online softmax, and the register that can't move", section "Online
@@ -15,6 +15,12 @@
 // base-2 domain, t = s * scale * log2(e), so every exponential is one ex2.
 //
 // GB300 mapping:
+//   * Persistent grid, one CTA per SM, each working through a sequence of query
+//     tiles: causal tiles paired long with short and dealt out statically for
+//     most of the work, the rest handed out one tile at a time from a global
+//     counter.  The TMA ring, the S/P double buffers and every barrier phase
+//     run on across tile boundaries, so the loads and first S products of the
+//     next tile overlap the end of this one.
 //   * S_j = Q K_j^T and O += P_j V_j run on tcgen05.mma (bf16 in, fp32
 //     accumulate) with the accumulators in tensor memory (TMEM).  S is double
 //     buffered and P has columns of its own, so S_{j+1} is computed while the
@@ -29,9 +35,15 @@
 //   * Q, K_j and V_j are brought in by TMA (128-byte swizzle) into rings of
 //     shared-memory stages guarded by mbarriers.
 //   * Warp roles: warp 0 issues TMA loads, warp 1 owns TMEM and issues the S
-//     products, warp 2 issues the P V products, warps 4-7 (one thread per
-//     query row) do the softmax, the O rescale on TMEM and the epilogue
-//     (O/l -> bf16 -> shared -> TMA store, LSE store).
+//     products, warp 2 issues the P V products, warps 4-11 do the softmax, the
+//     O rescale on TMEM and the epilogue (O/l -> bf16 -> global, LSE).  The
+//     softmax warps form two groups of four (one warp per 32-row TMEM lane
+//     quarter) that take alternate key tiles, a thread holding all 128 scores
+//     of its row.  Only the reference maximum passes from one step to the
+//     next; each group hands it to the other through shared memory as soon as
+//     its row maximum is known, so the exponentials of step j overlap the
+//     TMEM load and maximum of step j+1.  Each group keeps its row sums
+//     against the last reference it used; the two are combined at the end.
 //   * The reference maximum of a row moves only when the row maximum has
 //     grown past it by more than 64 in base-2 units; otherwise the old
 //     reference is kept, exponentials up to 2^64 are accumulated in fp32 and
@@ -58,10 +70,14 @@ namespace fa {
 
 constexpr int kBlockM = 128;   // query rows per tile = TMEM lanes
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 256;  // 8 warps
+constexpr int kThreads = 384;  // 12 warps
+constexpr int kSoftmaxWarps = 8;  // two groups of four, one warp per TMEM lane quarter each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kChunkBytes = 128u * 128u;  // one [128 rows][64 bf16] swizzled chunk
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kItemRing = 4;  // work items the producer may run ahead of the slowest role
+// readers of each posted work item: the two MMA issuers and every softmax warp
+constexpr int kItemReaders = 2 + 8;
 // Base-2 growth of a row's maximum tolerated before its reference moves.  It
 // bounds every exponential by 2^64, the row sums by N * 2^64 and |O| by
 // N * 2^64 * max|V|: finite in fp32 for max|V| < 2^33 at any N < 2^31.
@@ -80,12 +96,18 @@ enum : unsigned int {
     kStatusSelfTest = 1u << 8,
     kStatusMmaWaitSFree = 1u << 9,
     kStatusSoftmaxWaitPV = 1u << 10,
+    kStatusSoftmaxWaitX = 1u << 11,
+    kStatusItemWait = 1u << 12,
 };
 
 __device__ unsigned int g_fa_status = 0;
 
 struct FaParams {
-    float* lse;
+    void* o;     // bf16 [B*H][N][d]
+    float* lse;  // fp32 [B*H][N]
+    int BH;
+    int static_rounds;    // persistent schedule: rounds of tile pairs assigned statically per CTA
+    unsigned int* queue;  // persistent schedule: {next dynamic item, CTAs finished}, zero on entry, reset on exit
     int N;
     int n_tiles;       // ceil(N / 128) query (= key) tiles
     int causal;
@@ -104,12 +126,13 @@ struct FaSmem {
     static_assert(D == 64 || D == 128, "head dim");
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kTileBytes = kBlockN * D * 2;
-    static constexpr uint32_t kOffQ = 0;  // the query tile, later the O staging
-    static constexpr uint32_t kOffK = kOffQ + kTileBytes;
+    static constexpr int kQBufs = 1;      // query tiles in flight: the next tile's Q lands early
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffK = kOffQ + kQBufs * kTileBytes;
     static constexpr uint32_t kOffV = kOffK + NK * kTileBytes;
     static constexpr uint32_t kOffBar = kOffV + NV * kTileBytes;
-    static constexpr int kBarQ = 0;
-    static constexpr int kBarKFull = 1;
+    static constexpr int kBarQ = 0;  // per Q buffer: the tile landed
+    static constexpr int kBarKFull = kBarQ + kQBufs;
     static constexpr int kBarKEmpty = kBarKFull + NK;
     static constexpr int kBarVFull = kBarKEmpty + NK;
     static constexpr int kBarVEmpty = kBarVFull + NV;
@@ -117,13 +140,23 @@ struct FaSmem {
     static constexpr int kBarSFree = kBarSFull + 2;    // per S buffer: S_j read by the softmax
     static constexpr int kBarPFull = kBarSFree + 2;    // per P buffer: P_j written
     static constexpr int kBarPVDone = kBarPFull + 2;   // per P buffer: P_j V_j finished
-    static constexpr int kBarOFinal = kBarPVDone + 2;  // the last P V product finished
-    static constexpr int kBarDrain = kBarOFinal + 1;   // per MMA issuer
-    static constexpr int kNumBars = kBarDrain + 2;
-    static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+    static constexpr int kBarOFinal = kBarPVDone + 2;  // per tile: its last P V product finished
+    static constexpr int kBarQFree = kBarOFinal + 1;   // per Q buffer: the tile's last S product finished
+    static constexpr int kBarOFree = kBarQFree + kQBufs;  // per tile: O read out of TMEM (accumulator reusable)
+    static constexpr int kBarDrain = kBarOFree + 1;    // per MMA issuer
+    static constexpr int kBarXRef = kBarDrain + 2;     // per lane quarter and softmax group: reference handed over
+    static constexpr int kBarXSum = kBarXRef + 8;      // per lane quarter: both groups' row sums posted
+    static constexpr int kBarItemFull = kBarXSum + 4;  // per item-ring slot: the producer posted an item
+    static constexpr int kBarItemEmpty = kBarItemFull + kItemRing;  // per slot: every role has read it
+    static constexpr int kNumBars = kBarItemEmpty + kItemRing;
+    // references [2 groups][128 rows], then row states [2 tile parities][2 groups][m, l, l32][128 rows]
+    static constexpr uint32_t kOffXchg = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kOffItems = kOffXchg + (2 * kBlockM + 2 * 2 * 3 * kBlockM) * 4;  // int[kItemRing]
+    static constexpr uint32_t kOffTmemSlot = kOffItems + kItemRing * 4;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
     static constexpr uint32_t kBytes = kOffAbort + 4;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
+    static_assert(kAlloc <= 232448u, "dynamic shared memory above the 227 KB a CTA may use");
     // TMEM columns: S0 S1 O P0 P1
     __host__ __device__ static constexpr uint32_t col_s(int b) { return (uint32_t)b * 128u; }
     static constexpr uint32_t kColO = 256;
@@ -173,15 +206,16 @@ __device__ __forceinline__ bool fa_wait_drain(uint32_t bar, uint32_t parity, uin
     }
 }
 
-// Exponentials of one 128-key row tile against the reference -neg_m (base 2):
+// Exponentials of NE keys of a row against the reference -neg_m (base 2):
 // P packed to bf16 pairs, the sum of the bf16-rounded values and the fp32 sum.
-__device__ __forceinline__ void exp_row_tile(const float (&s)[kBlockN], float c2, float neg_m,
-                                             uint32_t (&pk)[kBlockN / 2], float& sum_bf, float& sum_f32) {
+template <int NE>
+__device__ __forceinline__ void exp_row_tile(const float (&s)[NE], float c2, float neg_m, uint32_t (&pk)[NE / 2],
+                                             float& sum_bf, float& sum_f32) {
     const uint64_t c2x2 = f32x2_pack(c2, c2), negm2 = f32x2_pack(neg_m, neg_m);
     float rs[4] = {0.f, 0.f, 0.f, 0.f};
     uint64_t r32[2] = {0ull, 0ull};  // packed (even, odd) fp32 partial sums
 #pragma unroll
-    for (int i = 0; i < kBlockN / 2; ++i) {
+    for (int i = 0; i < NE / 2; ++i) {
         float x0, x1;
         f32x2_unpack(ffma2(f32x2_pack(s[2 * i], s[2 * i + 1]), c2x2, negm2), x0, x1);
         const float p0 = ex2_approx(x0);
@@ -197,38 +231,183 @@ __device__ __forceinline__ void exp_row_tile(const float (&s)[kBlockN], float c2
     sum_f32 = (e0 + o0) + (e1 + o1);
 }
 
-// kSplit: the CTA covers only the key tiles of split blockIdx.z and writes the
+// One unit of work: query tile qt of head bh against key tiles j0 .. j0+n_kv-1.
+struct TileWork {
+    int qt, bh, j0, n_kv;
+};
+
+// Persistent schedule.  The query tiles of a head are paired, (n_tiles-1-i, i):
+// a long causal tile with a short one, so that every pair costs about the
+// same; pairs are numbered head-major (the CTAs busy at any moment share the
+// keys and values of a few heads in L2).  Each CTA first takes static_rounds
+// pairs statically (pairs blockIdx.x, blockIdx.x + gridDim.x, ...), which keeps
+// a pair's two tiles, and the shared keys and values, on one SM.  The
+// remaining pairs are split into single tiles that CTAs take one at a time
+// from a global counter -- first all their long tiles, then the short ones --
+// so that CTAs that ran faster (or got less) do more of the tail.
+__host__ __device__ inline long long persistent_pairs(const FaParams& p) {
+    return (long long)p.BH * ((p.n_tiles + 1) / 2);
+}
+
+__device__ inline void pair_tiles(const FaParams& p, long long pair, int& bh, int& qt_long, int& qt_short) {
+    const int per_head = (p.n_tiles + 1) / 2;
+    bh = (int)(pair / per_head);
+    const int i = (int)(pair % per_head);
+    qt_long = p.n_tiles - 1 - i;
+    qt_short = i;  // equal to qt_long for the middle tile of an odd count
+}
+
+__device__ inline void tile_work(const FaParams& p, int bh, int qt, TileWork& w) {
+    w.qt = qt;
+    w.bh = bh;
+    w.j0 = 0;
+    w.n_kv = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;
+}
+
+// The sequence of tiles one CTA processes; every role of the CTA walks its own
+// copy and sees the same tiles in the same order.
+//  * one-shot launch: the single tile (blockIdx.x from the last, longest
+//    causal tile down; blockIdx.y = head), restricted to the key split
+//    blockIdx.z when kSplit;
+//  * persistent launch: the producer warp chooses the tiles (choose()) and
+//    posts them, as bh * n_tiles + qt, in a shared-memory ring (produce()); the
+//    other roles read them from there (next()).  A negative entry ends the
+//    sequence.
+template <bool kSplit, bool kPersistent>
+struct TileSeq {
+    int n = 0;               // items taken so far
+    volatile int* ring;      // item ring in shared memory
+    uint32_t bar_full, bar_empty;
+    volatile int* abort_flag;
+    uint64_t limit;
+    __device__ TileSeq(volatile int* ring_, uint32_t full, uint32_t empty, volatile int* abort_, uint64_t limit_)
+        : ring(ring_), bar_full(full), bar_empty(empty), abort_flag(abort_), limit(limit_) {}
+
+    __device__ bool one_shot(const FaParams& p, TileWork& w) {
+        if (n > 0) return false;
+        n = 1;
+        w.qt = (int)gridDim.x - 1 - (int)blockIdx.x;
+        w.bh = (int)blockIdx.y;
+        const int n_all = p.causal ? min(w.qt + 1, p.n_tiles) : p.n_tiles;
+        w.j0 = 0;
+        w.n_kv = n_all;
+        if constexpr (kSplit) {
+            const int chunk = (n_all + p.n_splits - 1) / p.n_splits;
+            w.j0 = (int)blockIdx.z * chunk;
+            w.n_kv = max(0, min(n_all - w.j0, chunk));
+        }
+        return true;
+    }
+
+    // producer (one thread): choose the next tile and post it
+    int round = 0, sub = 0;  // static phase: pair round and tile within the pair
+    __device__ bool choose(const FaParams& p, int& bh, int& qt) {
+        while (round < p.static_rounds) {
+            int ql, qs;
+            pair_tiles(p, (long long)blockIdx.x + (long long)round * gridDim.x, bh, ql, qs);
+            if (sub == 0 || (sub == 1 && qs != ql)) {
+                qt = sub == 0 ? ql : qs;
+                ++sub;
+                return true;
+            }
+            sub = 0;
+            ++round;
+        }
+        const long long first = (long long)p.static_rounds * gridDim.x;  // first dynamic pair
+        const long long n_dyn = persistent_pairs(p) - first;
+        for (;;) {
+            const long long k = (long long)atomicAdd(p.queue, 1u);
+            if (k >= 2 * n_dyn) return false;
+            int ql, qs;
+            pair_tiles(p, first + (k < n_dyn ? k : k - n_dyn), bh, ql, qs);
+            if (k < n_dyn) {
+                qt = ql;
+                return true;
+            }
+            if (qs != ql) {
+                qt = qs;
+                return true;
+            }
+        }
+    }
+
+    __device__ bool produce(const FaParams& p, TileWork& w) {
+        if constexpr (!kPersistent) {
+            return one_shot(p, w);
+        } else {
+            const int s = n % kItemRing;
+            if (n >= kItemRing &&
+                !fa_wait(bar_empty + 8u * s, (uint32_t)(((n - kItemRing) / kItemRing) & 1), abort_flag, limit,
+                         kStatusItemWait))
+                return false;
+            int bh = 0, qt = 0;
+            const bool more = choose(p, bh, qt);
+            ring[s] = more ? bh * p.n_tiles + qt : -1;
+            mbar_arrive(bar_full + 8u * s);  // release: the ring entry is visible to the readers
+            ++n;
+            if (!more) return false;
+            tile_work(p, bh, qt, w);
+            return true;
+        }
+    }
+
+    // reader: a single thread (kWarp = false) or a whole warp (kWarp = true)
+    template <bool kWarp>
+    __device__ bool next(const FaParams& p, TileWork& w) {
+        if constexpr (!kPersistent) {
+            return one_shot(p, w);
+        } else {
+            const int s = n % kItemRing;
+            const uint32_t par = (uint32_t)((n / kItemRing) & 1);
+            const bool ok = kWarp ? fa_wait_warp(bar_full + 8u * s, par, abort_flag, limit, kStatusItemWait)
+                                  : fa_wait(bar_full + 8u * s, par, abort_flag, limit, kStatusItemWait);
+            if (!ok) return false;
+            const int item = ring[s];
+            if constexpr (kWarp) {
+                __syncwarp();
+                if ((threadIdx.x & 31) == 0) mbar_arrive(bar_empty + 8u * s);
+            } else {
+                mbar_arrive(bar_empty + 8u * s);
+            }
+            ++n;
+            if (item < 0) return false;
+            tile_work(p, item / p.n_tiles, item % p.n_tiles, w);
+            return true;
+        }
+    }
+};
+
+// kSplit: each CTA covers only the key tiles of split blockIdx.z and writes the
 // partial row state (m, both sums, unnormalised O) instead of O and LSE; a
 // merge kernel combines the splits ("5.2 CUDA Online Softmax", section 4.1:
 // the (m, d) merge is associative, so partial results combine in any order).
-template <int D, int NK, int NV, bool kSplit>
+// kPersistent: one CTA per SM walks a list of tiles; the TMA ring, the S and P
+// double buffers and all barrier phases continue across tile boundaries, so
+// the loads and first S products of the next tile overlap the end of this one.
+template <int D, int NK, int NV, bool kSplit, bool kPersistent>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                 const FaParams p) {
+                 const __grid_constant__ CUtensorMap tm_v, const FaParams p) {
     using L = FaSmem<D, NK, NV>;
+    using Seq = TileSeq<kSplit, kPersistent>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+    volatile int* items = reinterpret_cast<volatile int*>(smem + L::kOffItems);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
     auto bar = [&](int i) -> uint32_t { return sbase + L::kOffBar + 8u * (uint32_t)i; };
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = (int)(threadIdx.x & 31);
-    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest causal rows first
-    const int bh = (int)blockIdx.y;
-    const int n_all = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;  // key tiles this query tile sees
-    int j0 = 0, n_kv = n_all;  // this CTA's key tiles: j0 .. j0 + n_kv - 1
-    if constexpr (kSplit) {
-        const int chunk = (n_all + p.n_splits - 1) / p.n_splits;
-        j0 = (int)blockIdx.z * chunk;
-        n_kv = max(0, min(n_all - j0, chunk));
-    }
     const uint64_t limit = p.watchdog_ns;
 
     if (warp == 0 && lane == 0) {
-        mbar_init(bar(L::kBarQ), 1);
+#pragma unroll
+        for (int qb = 0; qb < L::kQBufs; ++qb) {
+            mbar_init(bar(L::kBarQ + qb), 1);
+            mbar_init(bar(L::kBarQFree + qb), 1);
+        }
 #pragma unroll
         for (int s = 0; s < NK; ++s) {
             mbar_init(bar(L::kBarKFull + s), 1);
@@ -242,18 +421,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::kBarSFull + b), 1);
-            mbar_init(bar(L::kBarSFree + b), 4);  // one arrival per softmax warp
-            mbar_init(bar(L::kBarPFull + b), 4);
+            mbar_init(bar(L::kBarSFree + b), kSoftmaxWarps / 2);  // one arrival per warp of group b
+            mbar_init(bar(L::kBarPFull + b), kSoftmaxWarps / 2);
             mbar_init(bar(L::kBarPVDone + b), 1);
             mbar_init(bar(L::kBarDrain + b), 1);
         }
         mbar_init(bar(L::kBarOFinal), 1);
+        mbar_init(bar(L::kBarOFree), kSoftmaxWarps);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mbar_init(bar(L::kBarXRef + i), 1);  // the handing-over warp
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mbar_init(bar(L::kBarXSum + i), 2);
+#pragma unroll
+        for (int i = 0; i < kItemRing; ++i) {
+            mbar_init(bar(L::kBarItemFull + i), 1);
+            mbar_init(bar(L::kBarItemEmpty + i), kItemReaders);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
-        prefetch_tensormap(&tm_o);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -266,48 +454,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------------
-        // TMA producer: Q once; K_0, K_1; then V_j and K_{j+2}, the order in
+        // TMA producer.  Per tile t: K_0; Q into buffer t % 2 once tile t-2's
+        // last S product has finished; K_1; then V_j and K_{j+2}: the order in
         // which the two MMA issuers consume them.
         // ------------------------------------------------------------------
-        if (lane == 0 && n_kv > 0) {
-            mbar_arrive_expect_tx(bar(L::kBarQ), L::kTileBytes);
-#pragma unroll
-            for (int c = 0; c < L::kChunks; ++c)
-                tma_load_3d(sbase + L::kOffQ + c * kChunkBytes, &tm_q, bar(L::kBarQ), c * 64, qt * kBlockM, bh);
-            int nk = 0, nv = 0;  // loads issued
-            auto load_k = [&](int j) -> bool {
-                const int s = j % NK;
-                const uint32_t r = (uint32_t)(j / NK);
+        if (lane == 0) {
+            int nk = 0, nv = 0, nq = 0;  // loads issued, over the whole tile sequence
+            auto load_k = [&](const TileWork& w, int j) -> bool {
+                const int s = nk % NK;
+                const uint32_t r = (uint32_t)(nk / NK);
                 if (!fa_wait(bar(L::kBarKEmpty + s), (r & 1u) ^ 1u, abort_flag, limit, kStatusLoadWait)) return false;
                 mbar_arrive_expect_tx(bar(L::kBarKFull + s), L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kOffK + s * L::kTileBytes + c * kChunkBytes, &tm_k, bar(L::kBarKFull + s),
-                                c * 64, (j0 + j) * kBlockN, bh);
+                                c * 64, (w.j0 + j) * kBlockN, w.bh);
                 ++nk;
                 return true;
             };
-            auto load_v = [&](int j) -> bool {
-                const int s = j % NV;
-                const uint32_t r = (uint32_t)(j / NV);
+            auto load_v = [&](const TileWork& w, int j) -> bool {
+                const int s = nv % NV;
+                const uint32_t r = (uint32_t)(nv / NV);
                 if (!fa_wait(bar(L::kBarVEmpty + s), (r & 1u) ^ 1u, abort_flag, limit, kStatusLoadWait)) return false;
                 mbar_arrive_expect_tx(bar(L::kBarVFull + s), L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_3d(sbase + L::kOffV + s * L::kTileBytes + c * kChunkBytes, &tm_v, bar(L::kBarVFull + s),
-                                c * 64, (j0 + j) * kBlockN, bh);
+                                c * 64, (w.j0 + j) * kBlockN, w.bh);
                 ++nv;
                 return true;
             };
-            bool ok = load_k(0);
-            if (ok && n_kv > 1) ok = load_k(1);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                ok = load_v(j);
-                if (ok && j + 2 < n_kv) ok = load_k(j + 2);
+            Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
+            TileWork w;
+            bool ok = true;
+            while (ok && seq.produce(p, w)) {
+                if (w.n_kv == 0) continue;
+                const int qb = nq % L::kQBufs;
+                ok = load_k(w, 0);
+                if (ok && nq >= L::kQBufs)
+                    ok = fa_wait(bar(L::kBarQFree + qb), (uint32_t)(((nq - L::kQBufs) / L::kQBufs) & 1), abort_flag,
+                                 limit, kStatusLoadWait);
+                if (ok) {
+                    mbar_arrive_expect_tx(bar(L::kBarQ + qb), L::kTileBytes);
+#pragma unroll
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma_load_3d(sbase + L::kOffQ + qb * L::kTileBytes + c * kChunkBytes, &tm_q, bar(L::kBarQ + qb),
+                                    c * 64, w.qt * kBlockM, w.bh);
+                    ++nq;
+                }
+                if (ok && w.n_kv > 1) ok = load_k(w, 1);
+                for (int j = 0; ok && j < w.n_kv; ++j) {
+                    ok = load_v(w, j);
+                    if (ok && j + 2 < w.n_kv) ok = load_k(w, j + 2);
+                }
             }
-            if (!ok) {
+            if (!ok || *abort_flag) {
                 // abort: let every copy already issued land before the CTA exits
-                fa_wait_drain(bar(L::kBarQ), 0, limit);
+                for (int qb = 0; qb < L::kQBufs; ++qb)
+                    if (nq > qb)
+                        fa_wait_drain(bar(L::kBarQ + qb), (uint32_t)(((nq - 1 - qb) / L::kQBufs) & 1), limit);
                 for (int s = 0; s < NK; ++s)
                     if (nk > s) fa_wait_drain(bar(L::kBarKFull + s), (uint32_t)(((nk - 1 - s) / NK) & 1), limit);
                 for (int s = 0; s < NV; ++s)
@@ -317,32 +522,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------------
-        // S issuer: S_j = Q K_j^T into buffer j % 2 once K_j has landed and
-        // the softmax has read S_{j-2} out of that buffer.
+        // S issuer: S_g = Q K_g^T into buffer g % 2 (g counts steps over the
+        // whole tile sequence) once K_g has landed and the softmax has read
+        // S_{g-2} out of that buffer.  After a tile's last S: commit QFree of
+        // its Q buffer.
         // ------------------------------------------------------------------
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
-            const uint32_t qa = sbase + L::kOffQ;
-            bool ok = n_kv > 0 && fa_wait(bar(L::kBarQ), 0, abort_flag, limit, kStatusMmaWaitQ);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int b = j & 1;
-                const int ks = j % NK;
-                if (j >= 2)
-                    ok = fa_wait(bar(L::kBarSFree + b), (uint32_t)(((j - 2) >> 1) & 1), abort_flag, limit,
-                                 kStatusMmaWaitSFree);
-                ok = ok && fa_wait(bar(L::kBarKFull + ks), (uint32_t)((j / NK) & 1), abort_flag, limit,
-                                   kStatusMmaWaitK);
-                if (!ok) break;
-                tc_fence_after_sync();
-                const uint32_t ka = sbase + L::kOffK + (uint32_t)ks * L::kTileBytes;
+            int g = 0, t = 0;
+            Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
+            TileWork w;
+            bool ok = true;
+            while (ok && seq.template next<false>(p, w)) {
+                if (w.n_kv == 0) continue;
+                const int qb = t % L::kQBufs;
+                const uint32_t qa = sbase + L::kOffQ + (uint32_t)qb * L::kTileBytes;
+                ok = fa_wait(bar(L::kBarQ + qb), (uint32_t)((t / L::kQBufs) & 1), abort_flag, limit, kStatusMmaWaitQ);
+                for (int j = 0; ok && j < w.n_kv; ++j, ++g) {
+                    const int b = g & 1;
+                    const int ks = g % NK;
+                    if (g >= 2)
+                        ok = fa_wait(bar(L::kBarSFree + b), (uint32_t)(((g - 2) >> 1) & 1), abort_flag, limit,
+                                     kStatusMmaWaitSFree);
+                    ok = ok && fa_wait(bar(L::kBarKFull + ks), (uint32_t)((g / NK) & 1), abort_flag, limit,
+                                       kStatusMmaWaitK);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t ka = sbase + L::kOffK + (uint32_t)ks * L::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + L::col_s(b), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                           kIdescS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
+                        mma_ss(tmem + L::col_s(b), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                               kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::kBarSFull + b));
+                    tc_commit(bar(L::kBarKEmpty + ks));
                 }
-                tc_commit(bar(L::kBarSFull + b));
-                tc_commit(bar(L::kBarKEmpty + ks));
+                if (ok) tc_commit(bar(L::kBarQFree + qb));  // the Q buffer may be refilled once these finish
+                ++t;
             }
             tc_commit(bar(L::kBarDrain + 0));  // every MMA must finish before TMEM is released
             fa_wait_drain(bar(L::kBarDrain + 0), 0, limit);
@@ -350,27 +567,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------------
-        // P V issuer: O += P_j V_j once P_j is in TMEM and V_j has landed.
+        // P V issuer: O += P_g V_g once P_g is in TMEM and V_g has landed; the
+        // first product of a tile (which overwrites O) also waits until the
+        // softmax warps have read the previous tile's O out of TMEM.
         // ------------------------------------------------------------------
         if (lane == 0) {
             constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+            int g = 0, t = 0;
+            Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
+            TileWork w;
             bool ok = true;
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int b = j & 1;
-                const int vs = j % NV;
-                ok = fa_wait(bar(L::kBarPFull + b), (uint32_t)((j >> 1) & 1), abort_flag, limit, kStatusMmaWaitP) &&
-                     fa_wait(bar(L::kBarVFull + vs), (uint32_t)((j / NV) & 1), abort_flag, limit, kStatusMmaWaitV);
-                if (!ok) break;
-                tc_fence_after_sync();
-                const uint32_t va = sbase + L::kOffV + (uint32_t)vs * L::kTileBytes;
+            while (ok && seq.template next<false>(p, w)) {
+                if (w.n_kv == 0) continue;
+                for (int j = 0; ok && j < w.n_kv; ++j, ++g) {
+                    const int b = g & 1;
+                    const int vs = g % NV;
+                    ok = fa_wait(bar(L::kBarPFull + b), (uint32_t)((g >> 1) & 1), abort_flag, limit,
+                                 kStatusMmaWaitP) &&
+                         fa_wait(bar(L::kBarVFull + vs), (uint32_t)((g / NV) & 1), abort_flag, limit,
+                                 kStatusMmaWaitV);
+                    if (ok && j == 0 && t > 0)
+                        ok = fa_wait(bar(L::kBarOFree), (uint32_t)((t - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t va = sbase + L::kOffV + (uint32_t)vs * L::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u,
-                           sdesc_sw128(va + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescPV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar(L::kBarVEmpty + vs));
-                tc_commit(bar(L::kBarPVDone + b));
-                if (j + 1 == n_kv) tc_commit(bar(L::kBarOFinal));
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u,
+                               sdesc_sw128(va + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescPV,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar(L::kBarVEmpty + vs));
+                    tc_commit(bar(L::kBarPVDone + b));
+                    if (j + 1 == w.n_kv) tc_commit(bar(L::kBarOFinal));
+                }
+                ++t;
             }
             tc_commit(bar(L::kBarDrain + 1));
             fa_wait_drain(bar(L::kBarDrain + 1), 0, limit);
@@ -378,117 +608,195 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------------
-        // Softmax / correction / epilogue: thread = one query row = TMEM lane.
+        // Softmax / correction / epilogue.  Thread = one query row (TMEM lane
+        // `row`).  The two warpgroups take alternate steps: group wg handles
+        // every step g with g % 2 == wg, all 128 keys of the row.  The online
+        // recurrence only threads the reference maximum from one step to the
+        // next, and that is handed over through shared memory right after the
+        // row maximum is known, so one group's exponentials overlap the other
+        // group's TMEM load and maximum of the following step.
         // ------------------------------------------------------------------
-        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+        const int quarter = warp & 3;    // TMEM lane quarter this warp may access
+        const int wg = (warp - 4) >> 2;  // warps 4-7: even steps, warps 8-11: odd steps
         const int row = quarter * 32 + lane;
-        const int q_idx = qt * kBlockM + row;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        float* xref = reinterpret_cast<float*>(smem + L::kOffXchg);  // [2 groups][128 rows]
+        float* xsum = xref + 2 * kBlockM;                              // [2 tile parities][2 groups][3][128 rows]
+        constexpr int kOCols = D / 2;  // O columns this thread stores in the epilogue
         const float c2 = p.scale_log2;
-        float m_run = -INFINITY;  // reference max, base-2 scaled units
-        float l_run = 0.f;        // sum of bf16(2^(t - m_run)): normalises O
-        float l32_run = 0.f;      // sum of 2^(t - m_run) in fp32: gives LSE
+        int g = 0, t = 0;  // steps and non-empty tiles so far
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int b = j & 1;
-            if (!fa_wait_warp(bar(L::kBarSFull + b), (uint32_t)((j >> 1) & 1), abort_flag, limit,
-                              kStatusSoftmaxWaitS)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            float s[kBlockN];
-            {
-                uint32_t r[kBlockN];
-                tmem_ld128_wait(t_lane + L::col_s(b), r);
-#pragma unroll
-                for (int i = 0; i < kBlockN; ++i) s[i] = __uint_as_float(r[i]);
-            }
-            // S_j is in registers: the buffer may take S_{j+2}
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarSFree + b));
-            // mask keys past the diagonal (causal) and past the end of the sequence
-            int lim = p.N - 1 - (j0 + j) * kBlockN;
-            if (p.causal && j0 + j == qt) lim = min(lim, row);
-            if (lim < kBlockN - 1) {
-#pragma unroll
-                for (int i = 0; i < kBlockN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
-            }
-            float mx[4] = {fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), fmax3(s[6], s[7], s[8]),
-                           fmax3(s[9], s[10], s[11])};
-#pragma unroll
-            for (int i = 12; i + 8 <= kBlockN; i += 8) {
-                mx[0] = fmax3(mx[0], s[i + 0], s[i + 1]);
-                mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
-                mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
-                mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
-            }
-            mx[0] = fmax3(mx[0], s[124], s[125]);
-            mx[1] = fmax3(mx[1], s[126], s[127]);
-            // scale > 0, so max(s) * c2 == max(s * c2)
-            const float m_cand = fmaxf(m_run, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2);
-            // move the reference only when the max grew past the threshold
-            // (always on the first visible tile: -inf + 64 = -inf < any finite max)
-            const bool move = m_cand > m_run + kRescaleThreshold;
-            const float alpha = move ? ex2_approx(m_run - m_cand) : 1.f;  // exp2(-inf) = 0 wipes the empty state
-            const bool any_move = __any_sync(0xffffffffu, move);
-            if (move) m_run = m_cand;
-            // a row with nothing visible yet keeps m = -inf and uses 0, so that its
-            // -inf scores give 0 rather than NaN
-            uint32_t pk[kBlockN / 2];
-            float sum_bf, sum_f32;
-            exp_row_tile(s, c2, (m_run == -INFINITY) ? 0.f : -m_run, pk, sum_bf, sum_f32);
-            l_run = l_run * alpha + sum_bf;
-            l32_run = l32_run * alpha + sum_f32;
-            if (j > 0 && any_move) {
-                // O must hold P_{j-1} V_{j-1} before it is rescaled
-                if (!fa_wait_warp(bar(L::kBarPVDone + (b ^ 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_flag, limit,
-                                  kStatusSoftmaxWaitPV)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32_wait(t_lane + L::kColO + 32u * c, r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st32(t_lane + L::kColO + 32u * c, r);
-                }
-            }
-            if (j >= 2) {
-                // P buffer b last fed P_{j-2} V_{j-2}: that product must have read it
-                if (!fa_wait_warp(bar(L::kBarPVDone + b), (uint32_t)(((j - 2) >> 1) & 1), abort_flag, limit,
-                                  kStatusSoftmaxWaitPV)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-            }
-            const uint32_t pcol = t_lane + L::col_p(b);
-            tmem_st32(pcol, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(pcol + 32u, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-            tmem_st_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarPFull + b));
-        }
-        if (ok && n_kv > 0) ok = fa_wait_warp(bar(L::kBarOFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
-        if constexpr (kSplit) {
-            // partial state of this split: unnormalised O and (m, sums) per row.
-            // The TMEM loads are warp-collective, so every lane runs them and
-            // only rows inside the sequence store.
+        Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
+        TileWork w;
+        while (ok && seq.template next<true>(p, w)) {
+            const int q_idx = w.qt * kBlockM + row;
             const bool valid = q_idx < p.N;
-            const size_t r = ((size_t)blockIdx.z * gridDim.y + (size_t)bh) * (size_t)p.N + (size_t)q_idx;
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + r * D);
-            if (ok && n_kv > 0) {
-                tc_fence_after_sync();
+            if constexpr (kSplit) {
+                if (w.n_kv == 0) {
+                    // no key of this split is visible: an empty partial state
+                    if (valid) {
+                        const size_t r = ((size_t)blockIdx.z * gridDim.y + (size_t)w.bh) * (size_t)p.N + (size_t)q_idx;
+                        float4* dst = reinterpret_cast<float4*>(p.ws_o + r * D + wg * kOCols);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                        for (int u = 0; u < kOCols / 4; ++u) dst[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (wg == 0) {
+                            p.ws_m[r] = -INFINITY;
+                            p.ws_lbf[r] = 0.f;
+                            p.ws_l32[r] = 0.f;
+                        }
+                    }
+                    continue;
+                }
+            }
+            float m_own = -INFINITY;  // reference this group's sums are relative to (base-2 units)
+            float l_run = 0.f;        // this group's sum of bf16(2^(t - m_own)): normalises O
+            float l32_run = 0.f;      // this group's fp32 sum of 2^(t - m_own): gives LSE
+            for (int j = 0; j < w.n_kv; ++j, ++g) {
+                if ((g & 1) != wg) continue;
+                const int b = wg;  // S and P buffer of this step
+                if (!fa_wait_warp(bar(L::kBarSFull + b), (uint32_t)((g >> 1) & 1), abort_flag, limit,
+                                  kStatusSoftmaxWaitS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                float s[kBlockN];
+                {
+                    uint32_t r[kBlockN];
+                    tmem_ld128_wait(t_lane + L::col_s(b), r);
+#pragma unroll
+                    for (int i = 0; i < kBlockN; ++i) s[i] = __uint_as_float(r[i]);
+                }
+                // S_g is in registers: the buffer may take S_{g+2}
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kBarSFree + b));
+                // mask keys past the diagonal (causal) and past the end of the sequence
+                int lim = p.N - 1 - (w.j0 + j) * kBlockN;
+                if (p.causal && w.j0 + j == w.qt) lim = min(lim, row);
+                if (lim < kBlockN - 1) {
+#pragma unroll
+                    for (int i = 0; i < kBlockN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+                }
+                float mx[4] = {fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), fmax3(s[6], s[7], s[8]),
+                               fmax3(s[9], s[10], s[11])};
+#pragma unroll
+                for (int i = 12; i + 8 <= kBlockN; i += 8) {
+                    mx[0] = fmax3(mx[0], s[i + 0], s[i + 1]);
+                    mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
+                    mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
+                    mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
+                }
+                mx[0] = fmax3(mx[0], s[124], s[125]);
+                mx[1] = fmax3(mx[1], s[126], s[127]);
+                const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                // reference after step g-1, handed over by the other group (every step
+                // after the first waits, so the hand-overs stay in lock step; a new
+                // tile starts from -inf and ignores the value)
+                float m_prev = -INFINITY;
+                if (g > 0) {
+                    if (!fa_wait_warp(bar(L::kBarXRef + quarter * 2 + (wg ^ 1)), (uint32_t)(((g - 1) >> 1) & 1),
+                                      abort_flag, limit, kStatusSoftmaxWaitX)) {
+                        ok = false;
+                        break;
+                    }
+                    const float v = xref[(wg ^ 1) * kBlockM + row];
+                    if (j > 0) m_prev = v;
+                }
+                // scale > 0, so max(s) * c2 == max(s * c2); the reference moves only
+                // when the max grew past it by more than the threshold (always on
+                // the first visible tile: -inf + 64 = -inf < any finite max)
+                const float m_cand = fmaxf(m_prev, row_max * c2);
+                const bool move = m_cand > m_prev + kRescaleThreshold;
+                const float m_new = move ? m_cand : m_prev;
+                xref[wg * kBlockM + row] = m_new;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kBarXRef + quarter * 2 + wg));
+                const bool any_move = __any_sync(0xffffffffu, move);
+                // bring this group's sums to the new reference (its last step may be
+                // two or more moves back)
+                const float a_l = (m_own == m_new) ? 1.f : ex2_approx(m_own - m_new);  // 2^-inf = 0
+                m_own = m_new;
+                // a row with nothing visible yet keeps m = -inf and uses 0, so that its
+                // -inf scores give 0 rather than NaN
+                uint32_t pk[kBlockN / 2];
+                float sum_bf, sum_f32;
+                exp_row_tile<kBlockN>(s, c2, (m_new == -INFINITY) ? 0.f : -m_new, pk, sum_bf, sum_f32);
+                l_run = l_run * a_l + sum_bf;
+                l32_run = l32_run * a_l + sum_f32;
+                if (g >= 2) {
+                    // P buffer b last fed P_{g-2} V_{g-2}: that product must have read it
+                    if (!fa_wait_warp(bar(L::kBarPVDone + b), (uint32_t)(((g - 2) >> 1) & 1), abort_flag, limit,
+                                      kStatusSoftmaxWaitPV)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                }
+                tmem_st64(t_lane + L::col_p(b), pk);
+                if (j > 0 && any_move) {
+                    // O must hold P_{g-1} V_{g-1} before it is rescaled; one load and
+                    // one store of the whole row (P is already out of the registers)
+                    if (!fa_wait_warp(bar(L::kBarPVDone + (b ^ 1)), (uint32_t)(((g - 1) >> 1) & 1), abort_flag,
+                                      limit, kStatusSoftmaxWaitPV)) {
+                        tmem_st_wait();  // the P store must complete before the CTA tears down
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const float a_o = move ? ex2_approx(m_prev - m_new) : 1.f;
+                    uint32_t r[D];
+                    if constexpr (D == 128)
+                        tmem_ld128_wait(t_lane + L::kColO, r);
+                    else
+                        tmem_ld64_wait(t_lane + L::kColO, r);
+#pragma unroll
+                    for (int i = 0; i < D; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a_o);
+                    if constexpr (D == 128)
+                        tmem_st128(t_lane + L::kColO, r);
+                    else
+                        tmem_st64(t_lane + L::kColO, r);
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kBarPFull + b));
+            }
+            if (!ok) break;
+            // whole-row state: both groups' sums brought to the later (larger) reference.
+            // Both warps of the pair evaluate the same expression in the same order.
+            float m_fin, l_fin, l32_fin;
+            {
+                float* xs = xsum + (size_t)(t & 1) * (2 * 3 * kBlockM);
+                xs[(wg * 3 + 0) * kBlockM + row] = m_own;
+                xs[(wg * 3 + 1) * kBlockM + row] = l_run;
+                xs[(wg * 3 + 2) * kBlockM + row] = l32_run;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kBarXSum + quarter));
+                ok = fa_wait_warp(bar(L::kBarXSum + quarter), (uint32_t)(t & 1), abort_flag, limit,
+                                  kStatusSoftmaxWaitX);
+                if (!ok) break;
+                const float m0 = xs[0 * kBlockM + row], m1 = xs[3 * kBlockM + row];
+                m_fin = fmaxf(m0, m1);
+                const float w0 = (m0 == m_fin) ? 1.f : ex2_approx(m0 - m_fin);
+                const float w1 = (m1 == m_fin) ? 1.f : ex2_approx(m1 - m_fin);
+                l_fin = xs[1 * kBlockM + row] * w0 + xs[4 * kBlockM + row] * w1;
+                l32_fin = xs[2 * kBlockM + row] * w0 + xs[5 * kBlockM + row] * w1;
+            }
+            ok = fa_wait_warp(bar(L::kBarOFinal), (uint32_t)(t & 1), abort_flag, limit, kStatusSoftmaxWaitO);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t o_col = t_lane + L::kColO + (uint32_t)(wg * kOCols);
+            if constexpr (kSplit) {
+                // partial state of this split: unnormalised O and (m, sums) per row.
+                // The TMEM loads are warp-collective: every lane runs them, only rows
+                // inside the sequence store.
+                const size_t r = ((size_t)blockIdx.z * gridDim.y + (size_t)w.bh) * (size_t)p.N + (size_t)q_idx;
+                float4* dst = reinterpret_cast<float4*>(p.ws_o + r * D + wg * kOCols);
+#pragma unroll
+                for (int c = 0; c < kOCols / 32; ++c) {
                     uint32_t v[32];
-                    tmem_ld32_wait(t_lane + L::kColO + 32u * c, v);
+                    tmem_ld32_wait(o_col + 32u * c, v);
                     if (valid) {
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
@@ -496,52 +804,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
                     }
                 }
-            } else if (ok && valid) {
-#pragma unroll
-                for (int u = 0; u < D / 4; ++u) dst[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            if (ok && valid) {
-                p.ws_m[r] = m_run;
-                p.ws_lbf[r] = l_run;
-                p.ws_l32[r] = l32_run;
-            }
-            tc_fence_before_sync();
-        } else {
-        // Q is dead once the last S product has finished (the softmax read it): stage O there
-        const uint32_t stage = sbase + L::kOffQ;
-        if (ok) {
-            tc_fence_after_sync();
-            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32_wait(t_lane + L::kColO + 32u * c, r);
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-                const uint32_t chunk = stage + (uint32_t)(c >> 1) * kChunkBytes + (uint32_t)row * 128u;
-#pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
-                    const uint32_t u = (uint32_t)((c & 1) * 4 + u4);  // 16-byte unit within the 128-byte row
-                    st_shared_v4(chunk + ((u ^ (uint32_t)(row & 7)) << 4), w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2],
-                                 w[4 * u4 + 3]);
+                if (valid && wg == 0) {
+                    p.ws_m[r] = m_fin;
+                    p.ws_lbf[r] = l_fin;
+                    p.ws_l32[r] = l32_fin;
                 }
-            }
-            if (q_idx < p.N)
-                p.lse[(size_t)bh * (size_t)p.N + (size_t)q_idx] =
-                    l32_run > 0.f ? (m_run + lg2_approx(l32_run)) * kLn2 : -INFINITY;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        named_barrier_sync(1, 128);
-        if (warp == 4 && lane == 0 && *abort_flag == 0) {
+            } else {
+                // O/l -> bf16, straight from registers to this thread's half row
+                const float inv_l = l_fin > 0.f ? 1.f / l_fin : 0.f;
+                uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                                       ((size_t)w.bh * (size_t)p.N + (size_t)q_idx) * D +
+                                                       wg * kOCols);
 #pragma unroll
-            for (int c = 0; c < L::kChunks; ++c) tma_store_3d(&tm_o, stage + c * kChunkBytes, c * 64, qt * kBlockM, bh);
-            bulk_commit_group();
-            bulk_wait_group_all();
+                for (int c = 0; c < kOCols / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32_wait(o_col + 32u * c, r);
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        wv[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+                    if (valid) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            orow[c * 4 + u] = make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
+                    }
+                }
+                if (valid && wg == 0)
+                    p.lse[(size_t)w.bh * (size_t)p.N + (size_t)q_idx] =
+                        l32_fin > 0.f ? (m_fin + lg2_approx(l32_fin)) * kLn2 : -INFINITY;
+            }
+            // O has been read out of TMEM: the next tile's first P V may overwrite it
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarOFree));
+            ++t;
         }
-        }  // kSplit
         __syncwarp();
     }
 
@@ -550,6 +847,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if constexpr (kPersistent) {
+        // the last CTA out leaves the counter at zero for the next launch
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(p.queue + 1, 1u) == gridDim.x - 1) {
+                atomicExch(p.queue + 0, 0u);
+                atomicExch(p.queue + 1, 0u);
+            }
+        }
     }
 }
 

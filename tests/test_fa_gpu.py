@@ -153,6 +153,35 @@ def test_deterministic_and_stream(fa):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_work_queue_across_calls_and_streams(fa):
+    """The persistent kernel takes tiles from a device work counter that every
+    launch leaves at zero: back-to-back calls, and calls overlapping on two
+    streams, must give exactly the results of the same calls run alone (every
+    tile's arithmetic is independent of which CTA runs it)."""
+    wa = wl.Workload("qa", 2, 8, 2048, 128, True, "iid", 11)   # 256 tiles: static pairs + dynamic tail
+    wb = wl.Workload("qb", 1, 4, 3000, 64, True, "iid", 12)    # ragged N, d = 64
+    qa, ka, va = (t.cuda() for t in wl.make_inputs(wa))
+    qb, kb, vb = (t.cuda() for t in wl.make_inputs(wb))
+    ref_a = fa.attention(qa, ka, va, causal=True)
+    ref_b = fa.attention(qb, kb, vb, causal=True)
+    torch.cuda.synchronize()
+    for _ in range(20):  # back to back on one stream
+        o, l = fa.attention(qa, ka, va, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_a[0]) and torch.equal(l, ref_a[1])
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(8):  # alternating streams, no synchronisation in between
+        with torch.cuda.stream(s1):
+            outs.append(("a", fa.attention(qa, ka, va, causal=True, stream=s1)))
+        with torch.cuda.stream(s2):
+            outs.append(("b", fa.attention(qb, kb, vb, causal=True, stream=s2)))
+    torch.cuda.synchronize()
+    for which, (o, l) in outs:
+        ro, rl = ref_a if which == "a" else ref_b
+        assert torch.equal(o, ro) and torch.equal(l, rl), which
+
+
 def test_inputs_untouched(fa):
     w = wl.Workload("ro", 1, 2, 300, 64, False, "iid", 6)
     q, k, v = (t.cuda() for t in wl.make_inputs(w))
