@@ -36,6 +36,8 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 tensor peak"
 FALLBACK_BF16_TFLOPS = 1900.0  # used only when MEASURED_PEAKS.json is absent
+FALLBACK_HBM_GBS = 6800.0
+SOFTMAX_METRIC = "row softmax GB/s (fp32, online normaliser, 1 GB300) and % of HBM copy bandwidth"
 KERNEL_NAME = "fa_fwd_sm103"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -75,14 +77,28 @@ def whole_job_tflops(world: int, flops_per_rank: float, steps: int, ms_total: fl
     return world * flops_per_rank * steps / (ms_total * 1e-3) / 1e12
 
 
-def measured_peak():
+class L2Flush:
+    """Evicts L2 between timed steps: writes a 512 MB buffer (more than L2), then
+    reads a second, 256 MB one, so that the dirty lines of the write are written
+    back before the timed region starts rather than during it."""
+
+    def __init__(self, torch, dev):
+        self.write = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        self.read = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.write.fill_(1)
+        self.read.sum()
+
+
+def measured_peak(key: str = "bf16_tflops"):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             j = json.load(f)
-        return float(j["bf16_tflops"]), "measured"
+        return float(j[key]), "measured"
     except Exception:
-        return FALLBACK_BF16_TFLOPS, "fallback"
+        return (FALLBACK_BF16_TFLOPS if key == "bf16_tflops" else FALLBACK_HBM_GBS), "fallback"
 
 
 def kernel_source_hash() -> str:
@@ -95,9 +111,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str = KERNEL_NAME):
     """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_traffic.txt")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
     if not os.path.exists(path):
         return None
     want = kernel_source_hash()
@@ -191,6 +207,144 @@ def cpu_baseline(w, q, k, v, target_s: float = 10.0):
             "sample": f"{n} seeded query rows of {w.name} (of {total}), fp64 three-pass route, {dt:.1f} s"}
 
 
+def run_softmax(args, rank, world, local_rank):
+    """The standalone row softmax: one step = one fa_softmax_rows call over an
+    M x N fp32 matrix (y and lse written).  value = algorithmic bytes (read x,
+    write y and lse: 8 M N + 4 M) / time."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    M, N = args.rows, args.cols
+    name = f"softmax-M{M}-N{N}-fp32"
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+
+        rng = np.random.default_rng(2000)
+        sample = max(1, min(M, int(os.environ.get("SOFTMAX_REF_ROWS", "256"))))
+        x = rng.standard_normal((sample, N), dtype=np.float32)
+        ms = []
+        for _ in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            for i in range(sample):
+                oracle.softmax_three_pass(x[i].astype(np.float64))
+            ms.append((time.perf_counter() - t0) * 1e3)
+        ms_step = statistics.mean(ms[args.warmup:])
+        value = (8.0 * sample * N + 4.0 * sample) / (ms_step * 1e-3) / 1e9
+        cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{sample} rows of {name} per step, fp64 three-pass route, one core"}
+        print(json.dumps({"impl": "reference", "metric": SOFTMAX_METRIC, "value": value, "unit": "GB/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": {"workload": name, "rows_per_step": sample},
+                          "cpu_baseline": cpu, "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                                       "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    if local_rank == 0:
+        __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    import online_softmax_04_gb300 as fa
+
+    rng = np.random.default_rng(2000 + rank)
+    hx = torch.from_numpy(rng.standard_normal((M, N), dtype=np.float32))
+    x = hx.to(dev)
+    y = torch.empty_like(x)
+    lse = torch.empty(M, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    algo_bytes = 8.0 * M * N + 4.0 * M
+    flush_l2 = algo_bytes < 2 * L2_BYTES
+    flusher = L2Flush(torch, dev) if flush_l2 else None
+
+    def step():
+        fa.fa_softmax_rows(x, y, lse, M, N, stream)
+
+    def timed(fn, n):
+        torch.cuda.synchronize()
+        if flush_l2:
+            ms = 0.0
+            for _ in range(n):
+                flusher()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ms += e0.elapsed_time(e1)
+            return ms
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    fa.fa_clear_device_status()
+    for _ in range(args.warmup):
+        step()
+    with ClockSampler(local_rank) as clk:
+        ms_total = timed(step, args.steps)
+    ms_step = ms_total / args.steps
+    value = algo_bytes / (ms_step * 1e-3) / 1e9
+    hxp = hx.pin_memory()
+    hy = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    hl = torch.empty(M, dtype=torch.float32, pin_memory=True)
+
+    def e2e_step():
+        x.copy_(hxp, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    ms_e2e = timed(e2e_step, args.steps) / args.steps
+    if fa.fa_get_device_status() != 0:
+        raise SystemExit("a softmax kernel gave up on a barrier")
+    if rank != 0:
+        return
+    peak, src = measured_peak("hbm_gbs")
+    if N % 4 == 0 and N <= 2048:
+        kernel = "softmax_rows_warp"
+    elif N % 4 == 0 and 4 * N <= 100 * 1024:
+        kernel = "softmax_rows_smem"
+    else:
+        kernel = "softmax_rows_stream"
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        sample = min(M, 512)
+        xs = hx[:sample].numpy().astype(np.float64)
+        t0 = time.perf_counter()
+        for i in range(sample):
+            oracle.softmax_three_pass(xs[i])
+        dt = time.perf_counter() - t0
+        cpu = {"value": (8.0 * sample * N + 4.0 * sample) / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{sample} rows of {name}, fp64 three-pass route, one core, {dt:.2f} s"}
+    line = {
+        "metric": SOFTMAX_METRIC, "value": value * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "M": M, "N": N, "bytes_per_step_per_gpu": algo_bytes,
+                   "l2": ("L2 flushed (512 MB write, then 256 MB read) before each individually timed step" if flush_l2 else
+                          "x and y larger than L2, back-to-back steps, no flush"),
+                   "entry_point": "fa_softmax_rows", "path": kernel},
+        "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "traffic": recorded_traffic(name, kernel), "peak_source": src, "kernel": kernel},
+        "cpu_baseline": cpu,
+        "e2e": {"value": algo_bytes * world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": 4 * M * N, "d2h_bytes_per_step": 4 * M * N + 4 * M, "ms_per_step": ms_e2e},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, w, rank, world):
     """The oracle as the reference arm: K timed steps, each a bounded row sample."""
     if rank != 0:
@@ -242,9 +396,17 @@ def main():
     ap.add_argument("--splitkv", type=int, default=-1,
                     help="use the split-KV entry point with this many splits (0 = automatic; default: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["attention", "softmax"], default="attention",
+                    help="attention (the headline) or the standalone row softmax")
+    ap.add_argument("--rows", type=int, default=4096, help="--op softmax: M")
+    ap.add_argument("--cols", type=int, default=4096, help="--op softmax: N")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.op == "softmax":
+        run_softmax(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+                    int(os.environ.get("LOCAL_RANK", "0")))
+        return
 
     from online_softmax_04_gb300 import workloads as wl
 
@@ -309,10 +471,10 @@ def main():
     torch.cuda.synchronize()
 
     # Inputs and outputs larger than L2 make back-to-back steps honest; smaller
-    # workloads get L2 flushed (a 512 MB write) before each individually timed step.
+    # workloads get L2 flushed (a 512 MB write, then a 256 MB read) before each individually timed step.
     io_bytes = 4 * q.numel() * q.element_size() + lse.numel() * lse.element_size()
     flush_l2 = io_bytes < 2 * L2_BYTES
-    scratch = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush_l2 else None
+    flusher = L2Flush(torch, dev) if flush_l2 else None
 
     def timed(fn, n):
         if dist is not None:
@@ -321,7 +483,7 @@ def main():
         if flush_l2:
             ms = 0.0
             for _ in range(n):
-                scratch.fill_(1)
+                flusher()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -389,7 +551,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                        "scale": "1/sqrt(d)", "flops_per_step_per_gpu": flops,
-                       "l2": ("L2 flushed (512 MB write) before each individually timed step" if flush_l2 else
+                       "l2": ("L2 flushed (512 MB write, then 256 MB read) before each individually timed step" if flush_l2 else
                               f"inputs larger than L2 ({io_bytes / 2**20:.0f} MiB of Q, K, V, O, LSE > 129 MB), "
                               "back-to-back steps, no flush"),
                        "parallelism": f"independent problem per GPU x{world}",

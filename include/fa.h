@@ -161,6 +161,32 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
  */
 int fa_splitkv_auto_splits(int B, int H, int N, int d, int causal);
 
+/*
+ * fa_softmax_rows -- row-wise softmax of an fp32 matrix with the online
+ * normaliser ("5.2 CUDA Online Softmax", sections 2 and 4.1; "Online softmax,
+ * and the register that can't move", section "Online softmax"):
+ *
+ *     y[i][j] = exp(x[i][j] - m_i) / d_i,     lse[i] = m_i + ln(d_i)
+ *
+ * with (m_i, d_i) the running max and running sum of exp(x - m) of row i,
+ * built in one pass and merged across threads with the associative rule.
+ *
+ *   x    : device fp32 [M][N], row-major, 4-byte aligned, read only.
+ *   y    : device fp32 [M][N], written.  May be x itself (in place); must not
+ *          overlap x otherwise.
+ *   lse  : device fp32 [M], written, or NULL.
+ *   M, N : rows and row length, >= 1 (M <= 2^40).
+ *
+ * Rows with N % 4 == 0, x and y 16-byte aligned and 4N <= 100 KiB are read
+ * from HBM once (bulk copies into shared memory: one warp per chunk of rows up
+ * to N = 2048, one CTA per row above); others are read twice.
+ * A row with no finite element gives y = 0 and lse = -inf; +inf or NaN in a row
+ * give NaN.  Returns FA_OK once the kernel is enqueued on `stream`, or
+ * FA_ERR_NULL_POINTER, FA_ERR_SHAPE, FA_ERR_ALIGNMENT, FA_ERR_ALIAS,
+ * FA_ERR_DEVICE, FA_ERR_CUDA.
+ */
+int fa_softmax_rows(const float* x, float* y, float* lse, long long M, int N, fa_stream_t stream);
+
 /* Human-readable name of an FA_* code; never NULL. */
 const char* fa_strerror(int code);
 

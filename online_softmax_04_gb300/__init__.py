@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
             L.fa_set_watchdog_ns.restype = ctypes.c_uint64
             L.fa_watchdog_selftest.argtypes = [ctypes.c_uint64, P, ctypes.POINTER(ctypes.c_uint)]
             L.fa_watchdog_selftest.restype = I
+            L.fa_softmax_rows.argtypes = [P, P, P, ctypes.c_longlong, I, P]
+            L.fa_softmax_rows.restype = I
             L.fa_version.argtypes = []
             L.fa_version.restype = I
             _lib = L
@@ -180,6 +182,27 @@ def attention_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
     fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, causal, (1.0 / math.sqrt(d)) if scale is None else scale, n_splits,
                    workspace, nbytes, stream)
     return o, lse
+
+
+def fa_softmax_rows(x, y, lse, M: int, N: int, stream=None) -> None:
+    """Enqueue the row softmax; raises FaError on a nonzero C return code."""
+    rc = lib().fa_softmax_rows(_ptr(x), _ptr(y), _ptr(lse), int(M), int(N), _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+
+
+def softmax(x, stream=None, out=None, with_lse: bool = True):
+    """x: CUDA fp32 [..., N].  Returns (y, lse) with lse None unless with_lse."""
+    import torch
+
+    if x.dtype != torch.float32:
+        raise ValueError("x must be float32")
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    y = torch.empty_like(x) if out is None else out
+    lse = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if with_lse else None
+    fa_softmax_rows(x, y, lse, M, N, stream)
+    return y, lse
 
 
 def fa_get_device_status() -> int:

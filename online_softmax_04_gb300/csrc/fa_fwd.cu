@@ -6,11 +6,13 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
 #include "../../include/fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "softmax_rows.cuh"
 
 namespace {
 
@@ -361,6 +363,51 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
     else
         fa::fa_splitkv_merge<128><<<blocks, 256, 0, s>>>(pr.p.ws_o, pr.p.ws_m, pr.p.ws_lbf, pr.p.ws_l32, ob, lse,
                                                          rows, n_splits);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_softmax_rows(const float* x, float* y, float* lse, long long M, int N, fa_stream_t stream) {
+    if (!x || !y) return FA_ERR_NULL_POINTER;
+    if (M < 1 || N < 1 || M > (1ll << 40)) return FA_ERR_SHAPE;
+    const uintptr_t ax = reinterpret_cast<uintptr_t>(x), ay = reinterpret_cast<uintptr_t>(y),
+                    al = reinterpret_cast<uintptr_t>(lse);
+    if (((ax | ay) & 3u) != 0 || (lse && (al & 3u) != 0)) return FA_ERR_ALIGNMENT;
+    const size_t bytes = (size_t)M * (size_t)N * 4u;
+    if (ax != ay && overlaps(x, bytes, y, bytes)) return FA_ERR_ALIAS;  // in place is fine, a shift is not
+    if (lse && (overlaps(lse, (size_t)M * 4u, x, bytes) || overlaps(lse, (size_t)M * 4u, y, bytes)))
+        return FA_ERR_ALIAS;
+    const int dev_rc = check_device();
+    if (dev_rc != FA_OK) return dev_rc;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    unsigned long long limit;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        limit = g_watchdog_ns;
+    }
+    const bool aligned = (N % 4 == 0) && ((ax | ay) & 15u) == 0;
+    if (aligned && N <= fa::kWarpMaxN) {
+        // short rows: one warp per chunk of rows
+        const long long chunks = (M + fa::warp_chunk_rows(N) - 1) / fa::warp_chunk_rows(N);
+        const long long ctas = (chunks + fa::kSmWarps - 1) / fa::kSmWarps;
+        if (ctas > 0x7fffffffll) return FA_ERR_SHAPE;
+        const size_t smem = (size_t)fa::kSmWarps * (fa::kWarpChunkBytes + 16u);
+        if (cudaFuncSetAttribute(fa::softmax_rows_warp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return FA_ERR_CUDA;
+        fa::softmax_rows_warp<<<(unsigned)ctas, fa::kSmThreads, smem, st>>>(x, y, lse, M, N, limit);
+    } else if (aligned && (size_t)N * 4u <= fa::kSmMaxRowBytes) {
+        // one CTA per row: the block scheduler keeps every SM full
+        const size_t smem = fa::softmax_rows_smem_bytes(N);
+        if (cudaFuncSetAttribute(fa::softmax_rows_smem, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return FA_ERR_CUDA;
+        const long long ctas = std::min<long long>(M, 0x7fffffffll);
+        fa::softmax_rows_smem<<<(unsigned)ctas, fa::kSmThreads, smem, st>>>(x, y, lse, M, N, limit);
+    } else {
+        const long long ctas = std::min<long long>(M, (long long)sms * 8);
+        fa::softmax_rows_stream<<<(unsigned)ctas, fa::kSmThreads, 0, st>>>(x, y, lse, M, N);
+    }
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

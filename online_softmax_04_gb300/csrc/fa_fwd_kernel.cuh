@@ -98,6 +98,7 @@ enum : unsigned int {
     kStatusSoftmaxWaitPV = 1u << 10,
     kStatusSoftmaxWaitX = 1u << 11,
     kStatusItemWait = 1u << 12,
+    kStatusSoftmaxRows = 1u << 13,
 };
 
 __device__ unsigned int g_fa_status = 0;

@@ -65,6 +65,22 @@ def test_host_validation(fa):
     assert call(fa, lse=FAKE + (3 << 30) + 64) == fa.FA_ERR_ALIAS  # lse overlaps o
 
 
+def test_softmax_rows_host_validation(fa):
+    L = fa.lib()
+    x, y, lse = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    assert L.fa_softmax_rows(0, y, lse, 4, 16, 0) == fa.FA_ERR_NULL_POINTER
+    assert L.fa_softmax_rows(x, 0, lse, 4, 16, 0) == fa.FA_ERR_NULL_POINTER
+    assert L.fa_softmax_rows(x, y, lse, 0, 16, 0) == fa.FA_ERR_SHAPE
+    assert L.fa_softmax_rows(x, y, lse, 4, 0, 0) == fa.FA_ERR_SHAPE
+    assert L.fa_softmax_rows(x, y, lse, (1 << 40) + 1, 1, 0) == fa.FA_ERR_SHAPE
+    assert L.fa_softmax_rows(x + 2, y, lse, 4, 16, 0) == fa.FA_ERR_ALIGNMENT
+    assert L.fa_softmax_rows(x, y, lse + 1, 4, 16, 0) == fa.FA_ERR_ALIGNMENT
+    assert L.fa_softmax_rows(x, x + 4, lse, 4, 16, 0) == fa.FA_ERR_ALIAS     # y shifted over x
+    assert L.fa_softmax_rows(x, y, x + 8, 4, 16, 0) == fa.FA_ERR_ALIAS       # lse inside x
+    if not torch.cuda.is_available():  # valid arguments, in place: no device to run on
+        assert L.fa_softmax_rows(x, x, 0, 4, 16, 0) in (fa.FA_ERR_CUDA, fa.FA_ERR_DEVICE)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="valid arguments would launch on a real GPU")
 def test_valid_arguments_without_a_gpu_fail_cleanly(fa):
     rc = call(fa)
