@@ -75,6 +75,9 @@ def _load():
             lib.oracle_attention_online.argtypes = [P, P, P, I64, I64, I64, I64, ctypes.c_int, D, I64, ctypes.c_int,
                                                     P, I64, P, P, ctypes.c_int]
             lib.oracle_attention_online.restype = ctypes.c_int
+            lib.oracle_attention_masked.argtypes = [P, P, P, I64, I64, I64, I64, D, I64, I64, P, P, I64, P, P,
+                                                    ctypes.c_int]
+            lib.oracle_attention_masked.restype = ctypes.c_int
             lib.oracle_softmax_three_pass.argtypes = [P, I64, P]
             lib.oracle_softmax_three_pass.restype = None
             lib.oracle_softmax_online.argtypes = [P, I64, P, P, P]
@@ -125,6 +128,30 @@ def attention_three_pass(q, k, v, causal: bool, scale: float, rows=None, n_threa
     if used < 0:
         raise ValueError(f"oracle rejected the arguments (code {used})")
     return (o, lse, used) if return_threads else (o, lse)
+
+
+def attention_masked(q, k, v, scale: float, window_left: int = -1, window_right: int = -1, doc_ids=None, rows=None,
+                     n_threads: int = 0):
+    """Three-pass attention where key j is visible to query i iff
+    (window_left < 0 or j >= i - window_left) and (window_right < 0 or
+    j <= i + window_right) and (doc_ids is None or doc_ids[b, i] == doc_ids[b, j]).
+    doc_ids: int32 [B, N] or None.  Returns O (n_rows, d) float64 and LSE (n_rows,)."""
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    B, H, N, d = q.shape
+    r = _rows_array(rows, B * H * N)
+    doc = None
+    if doc_ids is not None:
+        doc = np.ascontiguousarray(np.asarray(doc_ids), dtype=np.int32)
+        if doc.shape != (B, N):
+            raise ValueError("doc_ids must be [B, N]")
+    o = np.zeros((len(r), d), dtype=np.float64)
+    lse = np.zeros(len(r), dtype=np.float64)
+    used = _load().oracle_attention_masked(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, float(scale), int(window_left),
+                                           int(window_right), _ptr(doc) if doc is not None else None, _ptr(r), len(r),
+                                           _ptr(o), _ptr(lse), int(n_threads))
+    if used < 0:
+        raise ValueError(f"oracle rejected the arguments (code {used})")
+    return o, lse
 
 
 def attention_online(q, k, v, causal: bool, scale: float, tile: int = 128, rows=None, mutation: int = MUT_NONE,

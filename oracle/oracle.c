@@ -34,6 +34,13 @@
  *    row, and does not").  A tile of 1 is the scalar recurrence of the
  *    infra-guide page, section 2.1.
  *
+ *  - oracle_attention_masked: the three-pass route over the keys a general
+ *    mask leaves visible -- a window of keys around the query and, when
+ *    document ids are given, only keys of the query's own document (the
+ *    structured masks of "Online Softmax: Tiling Across a Reduction", causal
+ *    section, last paragraph).  The predicate is applied key by key; nothing
+ *    is skipped by blocks.
+ *
  * The softmax-only functions follow the infra-guide page: three-pass safe
  * softmax (section 1.1), the online recurrence (sections 2.1-2.2) and the
  * associative (m, d) merge (section 4.1).
@@ -211,6 +218,43 @@ void oracle_state_merge(double m1, double l1, const double* acc1, double m2, dou
     for (int64_t c = 0; c < d; ++c) acc[c] = acc1[c] * a1 + acc2[c] * a2;
 }
 
+/*
+ * Is key j visible to query i of batch b?  window_left < 0 / window_right < 0
+ * mean unbounded on that side; doc (int32 [B][N]) may be NULL.
+ */
+static int key_visible(int64_t b, int64_t i, int64_t j, int64_t N, int64_t window_left, int64_t window_right,
+                       const int32_t* doc) {
+    if (window_left >= 0 && j < i - window_left) return 0;
+    if (window_right >= 0 && j > i + window_right) return 0;
+    if (doc && doc[b * N + i] != doc[b * N + j]) return 0;
+    return 1;
+}
+
+/* Three-pass safe softmax over the visible keys of one row, then the weighted
+   sum of V.  No visible key: o = 0, lse = -inf. */
+static void row_three_pass_masked(const uint16_t* qrow, const uint16_t* kh, const uint16_t* vh, int64_t b, int64_t i,
+                                  int64_t N, int64_t d, double scale, int64_t wl, int64_t wr, const int32_t* doc,
+                                  double* xbuf, double* o, double* lse) {
+    for (int64_t j = 0; j < N; ++j)
+        xbuf[j] = key_visible(b, i, j, N, wl, wr, doc) ? score(qrow, kh + j * d, d, scale) : -INFINITY;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j) m = xbuf[j] > m ? xbuf[j] : m;
+    for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+    if (m == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) l += exp(xbuf[j] - m);
+    for (int64_t j = 0; j < N; ++j) {
+        if (xbuf[j] == -INFINITY) continue;
+        double w = exp(xbuf[j] - m) / l;
+        const uint16_t* vrow = vh + j * d;
+        for (int64_t c = 0; c < d; ++c) o[c] += w * bf16_bits_to_double(vrow[c]);
+    }
+    *lse = m + log(l);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Batched drivers: [B][H][N][d] bf16 tensors, rows given as bh*N + i.       */
 /* ------------------------------------------------------------------------ */
@@ -223,9 +267,11 @@ typedef struct {
     const int64_t* rows;
     int64_t n_rows;
     double *o, *lse;
-    int route; /* 0 three-pass, 1 online */
+    int route; /* 0 three-pass, 1 online, 2 three-pass under a general mask */
     int64_t tile;
     int mutation;
+    int64_t H, window_left, window_right;  /* route 2 */
+    const int32_t* doc;                     /* route 2: int32 [B][N] or NULL */
     int64_t next; /* shared work counter */
     pthread_mutex_t lock;
 } job_t;
@@ -252,6 +298,9 @@ static void* worker(void* arg) {
         double* o = jb->o + r * jb->d;
         if (jb->route == 0) {
             row_three_pass(qrow, kh, vh, nvis, jb->d, jb->scale, xbuf, o, jb->lse + r);
+        } else if (jb->route == 2) {
+            row_three_pass_masked(qrow, kh, vh, bh / jb->H, i, jb->N, jb->d, jb->scale, jb->window_left,
+                                  jb->window_right, jb->doc, xbuf, o, jb->lse + r);
         } else {
             double m, l;
             oracle_row_online_state(qrow, kh, vh, jb->d, 0, nvis, nvis, jb->tile, jb->scale, jb->mutation, &m, &l, o);
@@ -311,5 +360,20 @@ int oracle_attention_online(const uint16_t* q, const uint16_t* k, const uint16_t
     jb.q = q; jb.k = k; jb.v = v; jb.N = N; jb.d = d; jb.causal = causal; jb.scale = scale;
     jb.rows = rows; jb.n_rows = n_rows; jb.o = o; jb.lse = lse; jb.route = 1;
     jb.tile = tile; jb.mutation = mutation;
+    return run(&jb, n_threads);
+}
+
+/* Three-pass attention under a window and/or document mask (see key_visible). */
+int oracle_attention_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t B, int64_t H, int64_t N,
+                            int64_t d, double scale, int64_t window_left, int64_t window_right, const int32_t* doc,
+                            const int64_t* rows, int64_t n_rows, double* o, double* lse, int n_threads) {
+    if (!q || !k || !v || !rows || !o || !lse || B < 1 || H < 1 || N < 1 || d < 1) return -1;
+    for (int64_t r = 0; r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= B * H * N) return -2;
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.k = k; jb.v = v; jb.N = N; jb.d = d; jb.causal = 0; jb.scale = scale;
+    jb.rows = rows; jb.n_rows = n_rows; jb.o = o; jb.lse = lse; jb.route = 2;
+    jb.H = H; jb.window_left = window_left; jb.window_right = window_right; jb.doc = doc;
     return run(&jb, n_threads);
 }

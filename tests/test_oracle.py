@@ -352,3 +352,89 @@ def test_lse_shift_by_common_key_component():
         shift = (as_f64(q)[0, 0] @ u.astype(np.float64)) / 8
         assert np.max(np.abs(o1 - o2)) <= 1e-12
         assert np.max(np.abs(l2 - l1 - shift)) <= 1e-12
+
+
+# --------------------------------------------------------------------------
+# structured masks: window and document boundaries ("Online Softmax: Tiling
+# Across a Reduction", causal section, last paragraph)
+# --------------------------------------------------------------------------
+
+def doc_ids_from_lengths(B, N, lengths_per_batch):
+    doc = np.zeros((B, N), dtype=np.int32)
+    for b, lengths in enumerate(lengths_per_batch):
+        assert sum(lengths) == N
+        doc[b] = np.repeat(np.arange(len(lengths), dtype=np.int32), lengths)
+    return doc
+
+
+def test_masked_without_mask_is_full_and_right_window_zero_is_causal():
+    q, k, v = rand_qkv(1, 2, 70, 64, seed=21)
+    for causal, wr in ((False, -1), (True, 0)):
+        o_ref, l_ref = oracle.attention_three_pass(q, k, v, causal, 0.125)
+        o, lse = oracle.attention_masked(q, k, v, 0.125, window_left=-1, window_right=wr)
+        assert np.max(np.abs(o - o_ref)) <= 1e-14 and np.max(np.abs(lse - l_ref)) <= 1e-14
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_document_mask_equals_independent_documents(causal):
+    """A document mask is attention run separately on each document's slice."""
+    B, H, N, d = 2, 2, 96, 64
+    q, k, v = rand_qkv(B, H, N, d, seed=22)
+    lengths = [[30, 1, 65], [96]]
+    doc = doc_ids_from_lengths(B, N, lengths)
+    o, lse = oracle.attention_masked(q, k, v, 0.125, -1, 0 if causal else -1, doc)
+    o = o.reshape(B, H, N, d)
+    lse = lse.reshape(B, H, N)
+    for b in range(B):
+        start = 0
+        for n in lengths[b]:
+            sl = slice(start, start + n)
+            qs, ks, vs = (t[b:b + 1, :, sl].contiguous() for t in (q, k, v))
+            o_ref, l_ref = oracle.attention_three_pass(qs, ks, vs, causal, 0.125)
+            assert np.max(np.abs(o[b, :, sl].reshape(-1, d) - o_ref)) <= 1e-13
+            assert np.max(np.abs(lse[b, :, sl].reshape(-1) - l_ref)) <= 1e-13
+            start += n
+
+
+@pytest.mark.parametrize("wl,wr", [(0, 0), (5, 0), (16, 3), (40, -1), (-1, 7)])
+def test_window_row_equals_attention_over_its_keys(wl, wr):
+    """Row i under a window sees exactly keys [i - wl, i + wr] (clipped):
+    plain attention of that query over the key slice."""
+    B, H, N, d = 1, 1, 60, 64
+    q, k, v = rand_qkv(B, H, N, d, seed=23)
+    o, lse = oracle.attention_masked(q, k, v, 0.125, wl, wr)
+    for i in (0, 1, 17, 30, 59):
+        lo = 0 if wl < 0 else max(0, i - wl)
+        hi = N - 1 if wr < 0 else min(N - 1, i + wr)
+        ks, vs = k[:, :, lo:hi + 1].contiguous(), v[:, :, lo:hi + 1].contiguous()
+        qs = q[:, :, i:i + 1].expand(1, 1, hi - lo + 1, d).contiguous()  # every row = query i, full attention
+        o_ref, l_ref = oracle.attention_three_pass(qs, ks, vs, False, 0.125, rows=[0])
+        assert np.max(np.abs(o[i] - o_ref[0])) <= 1e-13 and abs(lse[i] - l_ref[0]) <= 1e-13
+
+
+def test_masks_brute_force_tiny():
+    """Window and document masks built independently (tril/triu bands and an
+    outer equality), softmax in long double."""
+    B, H, N, d = 2, 2, 33, 64
+    q, k, v = rand_qkv(B, H, N, d, seed=24, std=1.5)
+    doc = doc_ids_from_lengths(B, N, [[10, 23], [5, 5, 5, 18]])
+    qd, kd, vd = (as_f64(t).astype(np.longdouble) for t in (q, k, v))
+    S = np.einsum("bhid,bhjd->bhij", qd, kd) * np.longdouble(0.125)
+    for wl, wr, use_doc in ((4, 0, False), (3, 2, True), (-1, 0, True), (-1, -1, True)):
+        band = np.ones((N, N), dtype=bool)
+        if wl >= 0:
+            band &= np.triu(band, k=-wl)
+        if wr >= 0:
+            band &= np.tril(band, k=wr)
+        mask = np.broadcast_to(band, (B, H, N, N)).copy()
+        if use_doc:
+            mask &= (doc[:, None, :, None] == doc[:, None, None, :])
+        Sm = np.where(mask, S, np.longdouble(-np.inf))
+        m = Sm.max(axis=-1, keepdims=True)
+        P = np.exp(Sm - m)
+        l = P.sum(axis=-1, keepdims=True)
+        O = np.einsum("bhij,bhjd->bhid", P / l, vd).reshape(-1, d).astype(np.float64)
+        L = (m + np.log(l)).reshape(-1).astype(np.float64)
+        o, lse = oracle.attention_masked(q, k, v, 0.125, wl, wr, doc if use_doc else None)
+        assert np.max(np.abs(o - O)) <= 1e-12, (wl, wr, use_doc)
+        assert np.max(np.abs(lse - L)) <= 1e-12, (wl, wr, use_doc)
