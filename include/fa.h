@@ -62,7 +62,8 @@ enum {
     FA_ERR_DEVICE = -9,         /* the current device is not an sm_103 GPU */
     FA_ERR_SPLITS = -10,        /* n_splits outside 0..64 */
     FA_ERR_WORKSPACE = -11,     /* split-KV workspace smaller than fa_splitkv_workspace_bytes() */
-    FA_ERR_SCRATCH_LIMIT = -12  /* fa_fwd_splitkv_noalloc: partial states exceed FA_NOALLOC_SCRATCH_BYTES */
+    FA_ERR_SCRATCH_LIMIT = -12, /* fa_fwd_splitkv_noalloc: partial states exceed FA_NOALLOC_SCRATCH_BYTES */
+    FA_ERR_MASK = -13           /* fa_fwd_masked: a window bound below -1 */
 };
 
 /* Size of the library's static split-KV scratch used by fa_fwd_splitkv_noalloc (32 MiB). */
@@ -92,6 +93,36 @@ enum {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_fwd_masked -- fa_fwd under a structured mask: a sliding window and/or
+ * document boundaries ("Online Softmax: Tiling Across a Reduction", causal
+ * section: sliding windows and document-boundary masks become block-level
+ * skip decisions).  Key j is visible to query i of batch entry b iff
+ *
+ *     (window_left  < 0  or  j >= i - window_left)    and
+ *     (window_right < 0  or  j <= i + window_right)   and
+ *     (doc_ids == NULL   or  doc_ids[b][j] == doc_ids[b][i]).
+ *
+ * window_right = 0 is causal attention, window_left = W - 1 with it a causal
+ * sliding window of W keys; window_left = window_right = -1 with doc_ids NULL
+ * is fa_fwd non-causal.  Key tiles no row of a query tile can see are never
+ * loaded or multiplied; only tiles a boundary crosses are masked element by
+ * element.
+ *
+ *   window_left, window_right : -1 (unbounded) or >= 0.
+ *   doc_ids : device int32 [B][N], 4-byte aligned, or NULL.  The ids must not
+ *             decrease along a sequence (each document is one contiguous run of
+ *             positions); other ids give undefined results, never an
+ *             out-of-bounds access.
+ *   other arguments : as fa_fwd (there is no causal flag: use window_right).
+ *
+ * Every row sees at least itself.  Returns FA_OK, an fa_fwd argument error,
+ * FA_ERR_MASK for a window bound below -1, FA_ERR_ALIGNMENT for doc_ids, or
+ * FA_ERR_ALIAS when doc_ids overlaps o or lse.
+ */
+int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  int window_left, int window_right, const int32_t* doc_ids, float scale, fa_stream_t stream);
 
 /*
  * fa_fwd_splitkv -- the same forward for problems with few query tiles.

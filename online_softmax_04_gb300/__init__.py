@@ -32,6 +32,7 @@ FA_ERR_DEVICE = -9
 FA_ERR_SPLITS = -10
 FA_ERR_WORKSPACE = -11
 FA_ERR_SCRATCH_LIMIT = -12
+FA_ERR_MASK = -13
 FA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lock = threading.Lock()
@@ -56,6 +57,8 @@ def lib() -> ctypes.CDLL:
             P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             L.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P]
             L.fa_fwd.restype = I
+            L.fa_fwd_masked.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, F, P]
+            L.fa_fwd_masked.restype = I
             L.fa_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, ctypes.c_size_t, P]
             L.fa_fwd_splitkv.restype = I
             L.fa_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P]
@@ -130,6 +133,35 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, B, H, N, d, causal, (1.0 / math.sqrt(d)) if scale is None else scale, stream)
+    return o, lse
+
+
+def fa_fwd_masked(q, k, v, o, lse, B: int, H: int, N: int, d: int, window_left: int, window_right: int, doc_ids,
+                  scale: float, stream=None) -> None:
+    """Enqueue the masked forward (window and/or document ids); raises FaError on a nonzero C return code."""
+    rc = lib().fa_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
+                             int(window_left), int(window_right), _ptr(doc_ids), float(scale), _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+
+
+def attention_masked(q, k, v, window_left: int = -1, window_right: int = -1, doc_ids=None, scale: float | None = None,
+                     stream=None):
+    """q, k, v: CUDA bf16 [B, H, N, d]; doc_ids: CUDA int32 [B, N] or None.
+    Returns (o bf16 [B,H,N,d], lse fp32 [B,H,N])."""
+    import torch
+
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("q, k and v must be bfloat16")
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    if doc_ids is not None and (doc_ids.dtype != torch.int32 or tuple(doc_ids.shape) != (B, N)):
+        raise ValueError("doc_ids must be int32 [B, N]")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd_masked(q, k, v, o, lse, B, H, N, d, window_left, window_right, doc_ids,
+                  (1.0 / math.sqrt(d)) if scale is None else scale, stream)
     return o, lse
 
 

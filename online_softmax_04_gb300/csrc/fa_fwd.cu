@@ -154,6 +154,10 @@ int prepare(const void* q, const void* k, const void* v, void* o, float* lse, in
     p.o = o;
     p.lse = lse;
     p.BH = (int)BH;
+    p.H = H;
+    p.window_left = -1;
+    p.window_right = causal ? 0 : -1;
+    p.doc = nullptr;
     p.N = N;
     p.n_tiles = (N + fa::kBlockN - 1) / fa::kBlockN;
     p.causal = causal ? 1 : 0;
@@ -245,6 +249,29 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     Prepared pr;
     rc = prepare(q, k, v, o, lse, B, H, N, d, causal, scale, &pr);
     if (rc != FA_OK) return rc;
+    rc = queue_slot(&pr.p.queue);
+    if (rc != FA_OK) return rc;
+    return launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  int window_left, int window_right, const int32_t* doc_ids, float scale, fa_stream_t stream) {
+    int rc = validate(q, k, v, o, lse, B, H, N, d, scale);
+    if (rc != FA_OK) return rc;
+    if (window_left < -1 || window_right < -1) return FA_ERR_MASK;
+    if (doc_ids) {
+        if ((reinterpret_cast<uintptr_t>(doc_ids) & 3u) != 0) return FA_ERR_ALIGNMENT;
+        const size_t doc_bytes = (size_t)B * (size_t)N * 4u;
+        const size_t tensor_bytes = (size_t)B * H * (size_t)N * (size_t)d * 2u;
+        if (overlaps(doc_ids, doc_bytes, o, tensor_bytes) || overlaps(doc_ids, doc_bytes, lse, (size_t)B * H * N * 4u))
+            return FA_ERR_ALIAS;
+    }
+    Prepared pr;
+    rc = prepare(q, k, v, o, lse, B, H, N, d, window_right == 0 ? 1 : 0, scale, &pr);
+    if (rc != FA_OK) return rc;
+    pr.p.window_left = window_left;
+    pr.p.window_right = window_right;
+    pr.p.doc = doc_ids;
     rc = queue_slot(&pr.p.queue);
     if (rc != FA_OK) return rc;
     return launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, reinterpret_cast<cudaStream_t>(stream));
@@ -427,6 +454,7 @@ const char* fa_strerror(int code) {
         case FA_ERR_WORKSPACE: return "the split-KV workspace is smaller than fa_splitkv_workspace_bytes()";
         case FA_ERR_SCRATCH_LIMIT:
             return "the partial states need more than FA_NOALLOC_SCRATCH_BYTES; call fa_fwd_splitkv with a workspace";
+        case FA_ERR_MASK: return "window_left and window_right must be -1 (unbounded) or >= 0";
         default: return "unknown error code";
     }
 }

@@ -107,6 +107,12 @@ struct FaParams {
     void* o;     // bf16 [B*H][N][d]
     float* lse;  // fp32 [B*H][N]
     int BH;
+    int H;                // heads per batch entry (b = bh / H)
+    // key j is visible to query i iff j >= i - window_left (window_left >= 0),
+    // j <= i + window_right (window_right >= 0) and, with doc, doc[b][j] ==
+    // doc[b][i]; -1 leaves a side unbounded.  Causal attention: window_right = 0.
+    int window_left, window_right;
+    const int* doc;       // int32 [B][N] document ids, non-decreasing along each sequence, or nullptr
     int static_rounds;    // persistent schedule: rounds of tile pairs assigned statically per CTA
     unsigned int* queue;  // persistent schedule: {next dynamic item, CTAs finished}, zero on entry, reset on exit
     int N;
@@ -152,8 +158,9 @@ struct FaSmem {
     static constexpr int kNumBars = kBarItemEmpty + kItemRing;
     // references [2 groups][128 rows], then row states [2 tile parities][2 groups][m, l, l32][128 rows]
     static constexpr uint32_t kOffXchg = kOffBar + kNumBars * 8;
-    static constexpr uint32_t kOffItems = kOffXchg + (2 * kBlockM + 2 * 2 * 3 * kBlockM) * 4;  // int[kItemRing]
-    static constexpr uint32_t kOffTmemSlot = kOffItems + kItemRing * 4;
+    // work-item ring: per entry {bh * n_tiles + qt, first key tile, key tiles, unused}
+    static constexpr uint32_t kOffItems = kOffXchg + (2 * kBlockM + 2 * 2 * 3 * kBlockM) * 4;
+    static constexpr uint32_t kOffTmemSlot = kOffItems + kItemRing * 16;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
     static constexpr uint32_t kBytes = kOffAbort + 4;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
@@ -258,11 +265,49 @@ __device__ inline void pair_tiles(const FaParams& p, long long pair, int& bh, in
     qt_short = i;  // equal to qt_long for the middle tile of an odd count
 }
 
+// Document boundaries by binary search over non-decreasing ids (indices stay
+// within [0, N) whatever the ids hold): the first and the last position of the
+// document of position i.
+__device__ inline int doc_first(const int* d, int i) {
+    const int v = __ldg(d + i);
+    int lo = 0, hi = i;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(d + mid) < v) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+__device__ inline int doc_last(const int* d, int i, int N) {
+    const int v = __ldg(d + i);
+    int lo = i, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(d + mid) > v) hi = mid - 1; else lo = mid;
+    }
+    return lo;
+}
+
+// The key tiles query tile qt of head bh has to visit.  The first and last
+// visible key of a row never decrease with the row (windows slide, documents
+// are contiguous), so the tile's range runs from its first row's first key to
+// its last row's last key; tiles outside it are never visited ("Online
+// Softmax: Tiling Across a Reduction", causal section: masks become block-level
+// skip decisions).
 __device__ inline void tile_work(const FaParams& p, int bh, int qt, TileWork& w) {
     w.qt = qt;
     w.bh = bh;
-    w.j0 = 0;
-    w.n_kv = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;
+    const int r0 = qt * kBlockM, r1 = min(r0 + kBlockM, p.N) - 1;
+    int lo = 0, hi = p.N - 1;
+    if (p.window_left >= 0) lo = max(lo, r0 - p.window_left);
+    if (p.window_right >= 0) hi = min(hi, r1 + p.window_right);
+    if (p.doc) {
+        const int* d = p.doc + (size_t)(bh / p.H) * (size_t)p.N;
+        lo = max(lo, doc_first(d, r0));
+        hi = min(hi, doc_last(d, r1, p.N));
+    }
+    w.j0 = lo / kBlockN;
+    w.n_kv = hi >= lo ? hi / kBlockN - w.j0 + 1 : 0;
 }
 
 // The sequence of tiles one CTA processes; every role of the CTA walks its own
@@ -270,14 +315,14 @@ __device__ inline void tile_work(const FaParams& p, int bh, int qt, TileWork& w)
 //  * one-shot launch: the single tile (blockIdx.x from the last, longest
 //    causal tile down; blockIdx.y = head), restricted to the key split
 //    blockIdx.z when kSplit;
-//  * persistent launch: the producer warp chooses the tiles (choose()) and
-//    posts them, as bh * n_tiles + qt, in a shared-memory ring (produce()); the
-//    other roles read them from there (next()).  A negative entry ends the
-//    sequence.
+//  * persistent launch: the producer warp chooses the tiles (choose()),
+//    works out their key ranges (tile_work()) and posts both in a
+//    shared-memory ring (produce()); the other roles read them from there
+//    (next()).  A negative entry ends the sequence.
 template <bool kSplit, bool kPersistent>
 struct TileSeq {
     int n = 0;               // items taken so far
-    volatile int* ring;      // item ring in shared memory
+    volatile int* ring;      // item ring in shared memory, 4 ints per entry
     uint32_t bar_full, bar_empty;
     volatile int* abort_flag;
     uint64_t limit;
@@ -343,12 +388,13 @@ struct TileSeq {
                 return false;
             int bh = 0, qt = 0;
             const bool more = choose(p, bh, qt);
-            ring[s] = more ? bh * p.n_tiles + qt : -1;
+            if (more) tile_work(p, bh, qt, w);  // the key range is worked out once, here
+            ring[4 * s + 0] = more ? bh * p.n_tiles + qt : -1;
+            ring[4 * s + 1] = more ? w.j0 : 0;
+            ring[4 * s + 2] = more ? w.n_kv : 0;
             mbar_arrive(bar_full + 8u * s);  // release: the ring entry is visible to the readers
             ++n;
-            if (!more) return false;
-            tile_work(p, bh, qt, w);
-            return true;
+            return more;
         }
     }
 
@@ -363,7 +409,7 @@ struct TileSeq {
             const bool ok = kWarp ? fa_wait_warp(bar_full + 8u * s, par, abort_flag, limit, kStatusItemWait)
                                   : fa_wait(bar_full + 8u * s, par, abort_flag, limit, kStatusItemWait);
             if (!ok) return false;
-            const int item = ring[s];
+            const int item = ring[4 * s + 0], j0 = ring[4 * s + 1], n_kv = ring[4 * s + 2];
             if constexpr (kWarp) {
                 __syncwarp();
                 if ((threadIdx.x & 31) == 0) mbar_arrive(bar_empty + 8u * s);
@@ -372,7 +418,10 @@ struct TileSeq {
             }
             ++n;
             if (item < 0) return false;
-            tile_work(p, item / p.n_tiles, item % p.n_tiles, w);
+            w.qt = item % p.n_tiles;
+            w.bh = item / p.n_tiles;
+            w.j0 = j0;
+            w.n_kv = n_kv;
             return true;
         }
     }
@@ -649,6 +698,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
             }
+            // this row's visible keys, [row_lo, row_hi] (sequence positions), before documents;
+            // rows past N see every key (they are never stored)
+            int row_lo = 0, row_hi = p.N - 1, my_doc = 0;
+            if (valid) {
+                if (p.window_left >= 0) row_lo = max(0, q_idx - p.window_left);
+                if (p.window_right >= 0) row_hi = min(row_hi, q_idx + p.window_right);
+                if (p.doc) my_doc = __ldg(p.doc + (size_t)(w.bh / p.H) * (size_t)p.N + q_idx);
+            }
             float m_own = -INFINITY;  // reference this group's sums are relative to (base-2 units)
             float l_run = 0.f;        // this group's sum of bf16(2^(t - m_own)): normalises O
             float l32_run = 0.f;      // this group's fp32 sum of 2^(t - m_own): gives LSE
@@ -672,12 +729,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L::kBarSFree + b));
-                // mask keys past the diagonal (causal) and past the end of the sequence
-                int lim = p.N - 1 - (w.j0 + j) * kBlockN;
-                if (p.causal && w.j0 + j == w.qt) lim = min(lim, row);
-                if (lim < kBlockN - 1) {
+                // keys this row may see in this tile: [first, last] (tile-relative);
+                // past the end of the sequence, outside the window (causal: past the
+                // diagonal) and outside the row's document are masked
+                int first, last;
+                {
+                    const int k0 = (w.j0 + j) * kBlockN;
+                    first = row_lo - k0;
+                    last = min(row_hi, p.N - 1) - k0;
+                    if (p.doc && valid) {
+                        const int* dk = p.doc + (size_t)(w.bh / p.H) * (size_t)p.N + k0;
+                        const int cnt = min(kBlockN, p.N - k0);
+                        if (__ldg(dk) != my_doc || __ldg(dk + cnt - 1) != my_doc) {
+                            // a document boundary falls in this tile: the row's keys are
+                            // the run of its own id (lower and upper bound)
+                            int a = 0, e = cnt;
+                            while (a < e) {
+                                const int mid = (a + e) >> 1;
+                                if (__ldg(dk + mid) < my_doc) a = mid + 1; else e = mid;
+                            }
+                            int b2 = a, e2 = cnt;
+                            while (b2 < e2) {
+                                const int mid = (b2 + e2) >> 1;
+                                if (__ldg(dk + mid) <= my_doc) b2 = mid + 1; else e2 = mid;
+                            }
+                            first = max(first, a);
+                            last = min(last, b2 - 1);
+                        }
+                    }
+                }
+                if (first > 0 || last < kBlockN - 1) {
 #pragma unroll
-                    for (int i = 0; i < kBlockN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+                    for (int i = 0; i < kBlockN; ++i) s[i] = (i < first || i > last) ? -INFINITY : s[i];
                 }
                 float mx[4] = {fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), fmax3(s[6], s[7], s[8]),
                                fmax3(s[9], s[10], s[11])};

@@ -65,6 +65,24 @@ def test_host_validation(fa):
     assert call(fa, lse=FAKE + (3 << 30) + 64) == fa.FA_ERR_ALIAS  # lse overlaps o
 
 
+def test_masked_host_validation(fa):
+    L = fa.lib()
+    q, k, v, o, lse = FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30), FAKE + (4 << 30)
+    doc = FAKE + (5 << 30)
+
+    def m(wl=-1, wr=0, d=doc, N=128):
+        return L.fa_fwd_masked(q, k, v, o, lse, 1, 1, N, 64, wl, wr, d, 0.125, 0)
+
+    assert m(wl=-2) == fa.FA_ERR_MASK
+    assert m(wr=-7) == fa.FA_ERR_MASK
+    assert m(d=doc + 2) == fa.FA_ERR_ALIGNMENT
+    assert m(d=o + 64) == fa.FA_ERR_ALIAS            # ids inside o
+    assert m(N=0) == fa.FA_ERR_SHAPE
+    assert L.fa_fwd_masked(0, k, v, o, lse, 1, 1, 128, 64, -1, 0, None, 0.125, 0) == fa.FA_ERR_NULL_POINTER
+    if not torch.cuda.is_available():
+        assert m() in (fa.FA_ERR_CUDA, fa.FA_ERR_DEVICE)
+
+
 def test_softmax_rows_host_validation(fa):
     L = fa.lib()
     x, y, lse = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
