@@ -78,12 +78,12 @@ int sm_count();
 
 // kSplit: one CTA per (query tile, head, key split).  Otherwise a persistent
 // grid of at most one CTA per SM walks the work items (see fa::TileSeq).
-template <int D, int NK, int NV, bool kSplit>
+template <int D, int NK, int NV, bool kSplit, bool kMask = false>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, fa::FaParams p, int BH,
            cudaStream_t stream) {
     using L = fa::FaSmem<D, NK, NV>;
     constexpr bool kPersistent = !kSplit;
-    auto kern = fa::fa_fwd_sm103<D, NK, NV, kSplit, kPersistent>;
+    auto kern = fa::fa_fwd_sm103<D, NK, NV, kSplit, kPersistent, kMask>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
         return FA_ERR_CUDA;
     dim3 grid;
@@ -103,11 +103,11 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-template <bool kSplit>
+template <bool kSplit, bool kMask = false>
 int launch_d(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::FaParams& p,
              int BH, cudaStream_t s) {
-    if (d == 64) return launch<64, 6, 6, kSplit>(tq, tk, tv, p, BH, s);
-    return launch<128, 2, 3, kSplit>(tq, tk, tv, p, BH, s);
+    if (d == 64) return launch<64, 6, 6, kSplit, kMask>(tq, tk, tv, p, BH, s);
+    return launch<128, 2, 3, kSplit, kMask>(tq, tk, tv, p, BH, s);
 }
 
 struct Prepared {
@@ -274,7 +274,11 @@ int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* l
     pr.p.doc = doc_ids;
     rc = queue_slot(&pr.p.queue);
     if (rc != FA_OK) return rc;
-    return launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, reinterpret_cast<cudaStream_t>(stream));
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // full or causal attention without documents takes the unmasked kernel
+    if (window_left < 0 && (window_right < 0 || window_right == 0) && !doc_ids)
+        return launch_d<false, false>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, st);
+    return launch_d<false, true>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, st);
 }
 
 size_t fa_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits) {

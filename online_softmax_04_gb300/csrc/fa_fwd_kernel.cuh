@@ -294,9 +294,15 @@ __device__ inline int doc_last(const int* d, int i, int N) {
 // its last row's last key; tiles outside it are never visited ("Online
 // Softmax: Tiling Across a Reduction", causal section: masks become block-level
 // skip decisions).
+template <bool kMask>
 __device__ inline void tile_work(const FaParams& p, int bh, int qt, TileWork& w) {
     w.qt = qt;
     w.bh = bh;
+    if constexpr (!kMask) {  // full or causal attention
+        w.j0 = 0;
+        w.n_kv = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;
+        return;
+    }
     const int r0 = qt * kBlockM, r1 = min(r0 + kBlockM, p.N) - 1;
     int lo = 0, hi = p.N - 1;
     if (p.window_left >= 0) lo = max(lo, r0 - p.window_left);
@@ -319,7 +325,7 @@ __device__ inline void tile_work(const FaParams& p, int bh, int qt, TileWork& w)
 //    works out their key ranges (tile_work()) and posts both in a
 //    shared-memory ring (produce()); the other roles read them from there
 //    (next()).  A negative entry ends the sequence.
-template <bool kSplit, bool kPersistent>
+template <bool kSplit, bool kPersistent, bool kMask>
 struct TileSeq {
     int n = 0;               // items taken so far
     volatile int* ring;      // item ring in shared memory, 4 ints per entry
@@ -388,7 +394,7 @@ struct TileSeq {
                 return false;
             int bh = 0, qt = 0;
             const bool more = choose(p, bh, qt);
-            if (more) tile_work(p, bh, qt, w);  // the key range is worked out once, here
+            if (more) tile_work<kMask>(p, bh, qt, w);  // the key range is worked out once, here
             ring[4 * s + 0] = more ? bh * p.n_tiles + qt : -1;
             ring[4 * s + 1] = more ? w.j0 : 0;
             ring[4 * s + 2] = more ? w.n_kv : 0;
@@ -434,12 +440,12 @@ struct TileSeq {
 // kPersistent: one CTA per SM walks a list of tiles; the TMA ring, the S and P
 // double buffers and all barrier phases continue across tile boundaries, so
 // the loads and first S products of the next tile overlap the end of this one.
-template <int D, int NK, int NV, bool kSplit, bool kPersistent>
+template <int D, int NK, int NV, bool kSplit, bool kPersistent, bool kMask = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const FaParams p) {
     using L = FaSmem<D, NK, NV>;
-    using Seq = TileSeq<kSplit, kPersistent>;
+    using Seq = TileSeq<kSplit, kPersistent, kMask>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -701,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // this row's visible keys, [row_lo, row_hi] (sequence positions), before documents;
             // rows past N see every key (they are never stored)
             int row_lo = 0, row_hi = p.N - 1, my_doc = 0;
-            if (valid) {
+            if (kMask && valid) {
                 if (p.window_left >= 0) row_lo = max(0, q_idx - p.window_left);
                 if (p.window_right >= 0) row_hi = min(row_hi, q_idx + p.window_right);
                 if (p.doc) my_doc = __ldg(p.doc + (size_t)(w.bh / p.H) * (size_t)p.N + q_idx);
@@ -729,38 +735,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L::kBarSFree + b));
-                // keys this row may see in this tile: [first, last] (tile-relative);
-                // past the end of the sequence, outside the window (causal: past the
-                // diagonal) and outside the row's document are masked
-                int first, last;
-                {
-                    const int k0 = (w.j0 + j) * kBlockN;
-                    first = row_lo - k0;
-                    last = min(row_hi, p.N - 1) - k0;
-                    if (p.doc && valid) {
-                        const int* dk = p.doc + (size_t)(w.bh / p.H) * (size_t)p.N + k0;
-                        const int cnt = min(kBlockN, p.N - k0);
-                        if (__ldg(dk) != my_doc || __ldg(dk + cnt - 1) != my_doc) {
-                            // a document boundary falls in this tile: the row's keys are
-                            // the run of its own id (lower and upper bound)
-                            int a = 0, e = cnt;
-                            while (a < e) {
-                                const int mid = (a + e) >> 1;
-                                if (__ldg(dk + mid) < my_doc) a = mid + 1; else e = mid;
+                if constexpr (!kMask) {
+                    // mask keys past the diagonal (causal) and past the end of the sequence
+                    int lim = p.N - 1 - (w.j0 + j) * kBlockN;
+                    if (p.causal && w.j0 + j == w.qt) lim = min(lim, row);
+                    if (lim < kBlockN - 1) {
+#pragma unroll
+                        for (int i = 0; i < kBlockN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+                    }
+                } else {
+                    // keys this row may see in this tile: [first, last] (tile-relative);
+                    // past the end of the sequence, outside the window (causal: past the
+                    // diagonal) and outside the row's document are masked
+                    int first, last;
+                    {
+                        const int k0 = (w.j0 + j) * kBlockN;
+                        first = row_lo - k0;
+                        last = min(row_hi, p.N - 1) - k0;
+                        if (p.doc && valid) {
+                            const int* dk = p.doc + (size_t)(w.bh / p.H) * (size_t)p.N + k0;
+                            const int cnt = min(kBlockN, p.N - k0);
+                            if (__ldg(dk) != my_doc || __ldg(dk + cnt - 1) != my_doc) {
+                                // a document boundary falls in this tile: the row's keys are
+                                // the run of its own id (lower and upper bound)
+                                int a = 0, e = cnt;
+                                while (a < e) {
+                                    const int mid = (a + e) >> 1;
+                                    if (__ldg(dk + mid) < my_doc) a = mid + 1; else e = mid;
+                                }
+                                int b2 = a, e2 = cnt;
+                                while (b2 < e2) {
+                                    const int mid = (b2 + e2) >> 1;
+                                    if (__ldg(dk + mid) <= my_doc) b2 = mid + 1; else e2 = mid;
+                                }
+                                first = max(first, a);
+                                last = min(last, b2 - 1);
                             }
-                            int b2 = a, e2 = cnt;
-                            while (b2 < e2) {
-                                const int mid = (b2 + e2) >> 1;
-                                if (__ldg(dk + mid) <= my_doc) b2 = mid + 1; else e2 = mid;
-                            }
-                            first = max(first, a);
-                            last = min(last, b2 - 1);
                         }
                     }
-                }
-                if (first > 0 || last < kBlockN - 1) {
-#pragma unroll
-                    for (int i = 0; i < kBlockN; ++i) s[i] = (i < first || i > last) ? -INFINITY : s[i];
+                    if (first > 0 || last < kBlockN - 1) {
+    #pragma unroll
+                        for (int i = 0; i < kBlockN; ++i) s[i] = (i < first || i > last) ? -INFINITY : s[i];
+                    }
                 }
                 float mx[4] = {fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), fmax3(s[6], s[7], s[8]),
                                fmax3(s[9], s[10], s[11])};
