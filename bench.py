@@ -43,6 +43,11 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 def workload_flops(w) -> float:
+    """4 B H N^2 d, halved when causal; under a window or document mask, 4 d per visible (query, key) pair."""
+    if w.masked:
+        from online_softmax_04_gb300 import workloads as wl
+
+        return 4.0 * w.d * float(wl.visible_pairs(w))
     f = 4.0 * w.B * w.H * float(w.N) ** 2 * w.d
     return f / 2 if w.causal else f
 
@@ -51,9 +56,26 @@ def row_flops(w, rows) -> float:
     """The metric's FLOPs attributable to the given query rows: 4 d per visible key."""
     import numpy as np
 
+    if w.masked:
+        from online_softmax_04_gb300 import workloads as wl
+
+        return float(4.0 * w.d * wl.visible_per_row(w, rows).sum())
     i = np.asarray(rows) % w.N
     n_vis = (i + 1) if w.causal else np.full(len(i), w.N)
     return float(4.0 * w.d * n_vis.sum())
+
+
+def oracle_rows(w, q, k, v, rows, return_threads: bool = False):
+    """The oracle's three-pass route for the given rows, under the workload's mask if any."""
+    import oracle
+
+    if w.masked:
+        from online_softmax_04_gb300 import workloads as wl
+
+        o, lse = oracle.attention_masked(q, k, v, w.scale, w.window_left, w.window_right, wl.make_doc_ids(w),
+                                         rows=rows, n_threads=0)
+        return (o, lse, os.cpu_count() or 1) if return_threads else (o, lse)
+    return oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=rows, return_threads=return_threads)
 
 
 def rank_workload(w, rank: int):
@@ -196,12 +218,12 @@ def cpu_baseline(w, q, k, v, target_s: float = 10.0):
     perm = rng.permutation(total) if total <= 50_000_000 else rng.integers(0, total, size=1_000_000)
     n0 = min(256, total)
     t0 = time.perf_counter()
-    oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=perm[:n0])
+    oracle_rows(w, q, k, v, perm[:n0])
     t_cal = max(time.perf_counter() - t0, 1e-3)
     n = int(min(len(perm), max(n0, n0 * target_s / t_cal)))
     rows = perm[:n]
     t0 = time.perf_counter()
-    _, _, used = oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=rows, return_threads=True)
+    _, _, used = oracle_rows(w, q, k, v, rows, return_threads=True)
     dt = time.perf_counter() - t0
     return {"value": row_flops(w, rows) / dt / 1e12, "unit": "TFLOP/s", "cores": int(used), "kind": "oracle",
             "sample": f"{n} seeded query rows of {w.name} (of {total}), fp64 three-pass route, {dt:.1f} s"}
@@ -360,14 +382,14 @@ def run_reference(args, w, rank, world):
     rng = np.random.default_rng(w.seed + 5)
     total = w.B * w.H * w.N
     t0 = time.perf_counter()
-    oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=rng.integers(0, total, 128))
+    oracle_rows(w, q, k, v, rng.integers(0, total, 128))
     t_cal = max(time.perf_counter() - t0, 1e-3)
     n = int(max(128, 128 * per_step_s / t_cal))
     flops, secs, used = 0.0, 0.0, 1
     for step in range(args.warmup + args.steps):
         rows = rng.integers(0, total, n)
         t0 = time.perf_counter()
-        _, _, used = oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=rows, return_threads=True)
+        _, _, used = oracle_rows(w, q, k, v, rows, return_threads=True)
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             flops += row_flops(w, rows)
@@ -453,8 +475,16 @@ def main():
         ws_bytes = fa.fa_splitkv_workspace_bytes(w.B, w.H, w.N, w.d, n_splits)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
+    doc_dev = None
+    if w.masked:
+        docs = wl.make_doc_ids(w)
+        doc_dev = torch.from_numpy(docs).to(dev) if docs is not None else None
+
     def run_fwd():
-        if n_splits > 0:
+        if w.masked:
+            fa.fa_fwd_masked(dq, dk, dv, o, lse, w.B, w.H, w.N, w.d, w.window_left, w.window_right, doc_dev,
+                             w.scale, stream)
+        elif n_splits > 0:
             fa.fa_fwd_splitkv(dq, dk, dv, o, lse, w.B, w.H, w.N, w.d, w.causal, w.scale, n_splits, workspace,
                               ws_bytes, stream)
         else:
@@ -555,7 +585,10 @@ def main():
                               f"inputs larger than L2 ({io_bytes / 2**20:.0f} MiB of Q, K, V, O, LSE > 129 MB), "
                               "back-to-back steps, no flush"),
                        "parallelism": f"independent problem per GPU x{world}",
-                       "entry_point": "fa_fwd" if n_splits < 0 else f"fa_fwd_splitkv (n_splits={n_splits})"},
+                       "entry_point": ("fa_fwd_masked" if w.masked else "fa_fwd") if n_splits < 0
+                       else f"fa_fwd_splitkv (n_splits={n_splits})",
+                       **({"window_left": w.window_left, "window_right": w.window_right, "doc_mean": w.doc_mean,
+                           "flops": "4 d per visible (query, key) pair"} if w.masked else {})},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -19,6 +19,14 @@ Workloads (all with scale = 1/sqrt(d)):
   N(0,1) scaled by 0.25 + 3.75 j/(N-1), so the norms of the keys grow
   linearly along the sequence and large scores arrive late; V iid N(0,1).
 * ``B1-H8-N131072-d64-causal`` -- iid N(0,1), causal, long context.
+
+Structured masks (the window / document-boundary skips of "Online Softmax:
+Tiling Across a Reduction", causal section), run through ``fa_fwd_masked``:
+
+* ``B1-H32-N16384-d128-window4096`` -- iid N(0,1), causal sliding window of
+  4096 keys (window_left = 4095, window_right = 0).
+* ``B4-H16-N4096-d128-docs`` -- iid N(0,1), causal within packed documents:
+  seeded document lengths, uniform on [1, 2047] (mean 1024), per sequence.
 """
 from __future__ import annotations
 
@@ -39,6 +47,16 @@ class Workload:
     dist: str = "iid"            # iid | late | sorted | sorted-strict | zeros-q | onehot
     seed: int = 1000
     rows_per_head: int | None = None  # oracle rows checked per (b, h); None = every row
+    window_left: int = -1         # masked workloads: keys i - window_left .. (-1 = unbounded)
+    doc_mean: int = 0             # masked workloads: mean document length (0 = no documents)
+
+    @property
+    def masked(self) -> bool:
+        return self.window_left >= 0 or self.doc_mean > 0
+
+    @property
+    def window_right(self) -> int:
+        return 0 if self.causal else -1
 
     @property
     def scale(self) -> float:
@@ -58,6 +76,8 @@ WORKLOADS = {
         Workload("B4-H16-N4096-d128-causal", 4, 16, 4096, 128, True, "iid", 1002, 256),
         Workload("B1-H32-N16384-d128-causal-late", 1, 32, 16384, 128, True, "late", 1003, 256),
         Workload("B1-H8-N131072-d64-causal", 1, 8, 131072, 64, True, "iid", 1004, 64),
+        Workload("B1-H32-N16384-d128-window4096", 1, 32, 16384, 128, True, "iid", 1005, 64, window_left=4095),
+        Workload("B4-H16-N4096-d128-docs", 4, 16, 4096, 128, True, "iid", 1006, 64, doc_mean=1024),
     ]
 }
 
@@ -105,6 +125,65 @@ def make_inputs(w: Workload):
     else:
         raise ValueError(f"unknown distribution {w.dist!r}")
     return _to_bf16(q), _to_bf16(k), _to_bf16(v)
+
+
+def make_doc_ids(w: Workload):
+    """int32 [B, N] document ids for a workload with documents (None otherwise):
+    runs of seeded lengths uniform on [1, 2 doc_mean - 1], numbered 0, 1, ...
+    along each sequence."""
+    if w.doc_mean <= 0:
+        return None
+    rng = np.random.default_rng(w.seed + 31)
+    out = np.zeros((w.B, w.N), dtype=np.int32)
+    for b in range(w.B):
+        pos, doc = 0, 0
+        while pos < w.N:
+            n = int(rng.integers(1, 2 * w.doc_mean))
+            out[b, pos:pos + n] = doc
+            pos += n
+            doc += 1
+    return out
+
+
+def visible_pairs(w: Workload) -> int:
+    """Number of (query, key) pairs the mask leaves visible, over all B*H heads."""
+    N = w.N
+    docs = make_doc_ids(w)
+    total = 0
+    for b in range(w.B):
+        if docs is None:
+            starts, ends = np.array([0]), np.array([N])
+        else:
+            change = np.flatnonzero(np.diff(docs[b])) + 1
+            starts = np.concatenate([[0], change])
+            ends = np.concatenate([change, [N]])
+        for s0, e0 in zip(starts, ends):
+            n = int(e0 - s0)
+            i = np.arange(n, dtype=np.int64)
+            hi = i if w.causal else np.full(n, n - 1, dtype=np.int64)
+            lo = np.maximum(0, i - w.window_left) if w.window_left >= 0 else np.zeros(n, dtype=np.int64)
+            total += int(np.sum(hi - lo + 1))
+    return total * w.H
+
+
+def visible_per_row(w: Workload, rows) -> np.ndarray:
+    """Number of keys each given flat query row (bh * N + i) may see."""
+    rows = np.asarray(rows, dtype=np.int64)
+    N = w.N
+    i = rows % N
+    b = (rows // N) // w.H
+    lo = np.maximum(0, i - w.window_left) if w.window_left >= 0 else np.zeros(len(i), dtype=np.int64)
+    hi = i.copy() if w.causal else np.full(len(i), N - 1, dtype=np.int64)
+    docs = make_doc_ids(w)
+    if docs is not None:
+        for bb in np.unique(b):
+            sel = b == bb
+            d = docs[bb]
+            first = np.searchsorted(d, d[i[sel]], side="left")
+            last = np.searchsorted(d, d[i[sel]], side="right") - 1
+            lo[sel] = np.maximum(lo[sel], first)
+            hi[sel] = np.minimum(hi[sel], last)
+    return hi - lo + 1
 
 
 def onehot_inputs(B: int, H: int, N: int, d: int, c: float, seed: int = 7):

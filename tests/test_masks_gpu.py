@@ -130,3 +130,23 @@ def test_rejects_bad_masks(fa):
                            0) == fa.FA_ERR_ALIGNMENT
     assert L.fa_fwd_masked(p, p, p, o.data_ptr(), lse.data_ptr(), 1, 1, 128, 64, -1, 0, o.data_ptr(), 0.1,
                            0) == fa.FA_ERR_ALIAS
+
+
+@pytest.mark.parametrize("name", ["B1-H32-N16384-d128-window4096", "B4-H16-N4096-d128-docs"])
+def test_masked_workloads_sampled_rows(fa, name):
+    """The masked workloads bench.py measures, at full size, in the launch it times."""
+    w = wl.WORKLOADS[name]
+    q, k, v = wl.make_inputs(w)
+    docs = wl.make_doc_ids(w)
+    dev = torch.device("cuda:0")
+    o, lse = fa.attention_masked(q.to(dev), k.to(dev), v.to(dev), w.window_left, w.window_right,
+                                 torch.from_numpy(docs).to(dev) if docs is not None else None)
+    torch.cuda.synchronize()
+    rows = wl.sample_rows(w)
+    ref_o, ref_lse = oracle.attention_masked(q, k, v, w.scale, w.window_left, w.window_right, docs, rows=rows)
+    got_o = o.float().cpu().numpy().reshape(-1, w.d)[rows].astype(np.float64)
+    got_l = lse.cpu().numpy().reshape(-1)[rows].astype(np.float64)
+    err_o = np.abs(got_o - ref_o).max()
+    err_l = (np.abs(got_l - ref_lse) / np.maximum(1.0, np.abs(ref_lse))).max()
+    print(f"{name}: max|dO|={err_o:.3e} max rel dLSE={err_l:.3e} rows={len(rows)}")
+    assert err_o <= O_TOL and err_l <= LSE_TOL

@@ -51,3 +51,27 @@ def test_sample_rows():
     assert all(len(set(row)) == 256 for row in per.tolist())
     assert np.array_equal(r, wl.sample_rows(w))
     assert len(wl.sample_rows(wl.WORKLOADS["B1-H1-N4096-d64-full"])) == 4096
+
+
+def test_visible_pairs_match_a_brute_force_mask():
+    """Masked workloads count 4 d FLOPs per visible (query, key) pair; the count
+    must equal a mask built element by element."""
+    for w in (wl.Workload("t", 2, 3, 300, 64, True, "iid", 5, window_left=40),
+              wl.Workload("t", 2, 1, 257, 64, True, "iid", 6, doc_mean=30),
+              wl.Workload("t", 1, 2, 200, 64, False, "iid", 7, doc_mean=50),
+              wl.Workload("t", 1, 1, 150, 64, True, "iid", 8, window_left=9, doc_mean=20)):
+        docs = wl.make_doc_ids(w)
+        i = np.arange(w.N)[:, None]
+        j = np.arange(w.N)[None, :]
+        base = np.ones((w.N, w.N), dtype=bool)
+        if w.causal:
+            base &= j <= i
+        if w.window_left >= 0:
+            base &= j >= i - w.window_left
+        total = 0
+        for b in range(w.B):
+            m = base if docs is None else base & (docs[b][:, None] == docs[b][None, :])
+            total += int(m.sum()) * w.H
+        assert wl.visible_pairs(w) == total
+        rows = np.arange(w.B * w.H * w.N)
+        assert int(wl.visible_per_row(w, rows).sum()) == total
