@@ -78,6 +78,9 @@ def _load():
             lib.oracle_attention_masked.argtypes = [P, P, P, I64, I64, I64, I64, D, I64, I64, P, P, I64, P, P,
                                                     ctypes.c_int]
             lib.oracle_attention_masked.restype = ctypes.c_int
+            lib.oracle_attention_backward.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, D, P, I64,
+                                                      P, I64, P, P, P, P, P, P, ctypes.c_int]
+            lib.oracle_attention_backward.restype = ctypes.c_int
             lib.oracle_softmax_three_pass.argtypes = [P, I64, P]
             lib.oracle_softmax_three_pass.restype = None
             lib.oracle_softmax_online.argtypes = [P, I64, P, P, P]
@@ -152,6 +155,33 @@ def attention_masked(q, k, v, scale: float, window_left: int = -1, window_right:
     if used < 0:
         raise ValueError(f"oracle rejected the arguments (code {used})")
     return o, lse
+
+
+def attention_backward(q, k, v, o, dout, lse, causal: bool, scale: float, q_rows=None, k_rows=None,
+                       n_threads: int = 0):
+    """Gradients of L = sum(O * dO): dQ for the flat query rows q_rows, dK and dV
+    for the flat key rows k_rows (None = every row).  q, k, v: bf16 tensors
+    [B, H, N, d]; o, dout: the values the GPU sees, any float type, [B, H, N, d];
+    lse: natural-log statistic [B, H, N].  Returns a dict with dq, dk, dv and
+    their magnitudes mag_dq, mag_dk, mag_dv (sums of |term|), all float64."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, H, N, d = qb.shape
+    def f64(t, shape):  # torch tensors of any float type, or numpy arrays, widened exactly
+        a = t.detach().cpu().double().numpy() if hasattr(t, "detach") else np.asarray(t, dtype=np.float64)
+        return np.ascontiguousarray(a, dtype=np.float64).reshape(shape)
+
+    od, dod, ld = f64(o, (B, H, N, d)), f64(dout, (B, H, N, d)), f64(lse, (B, H, N))
+    qr = _rows_array(q_rows, B * H * N)
+    kr = _rows_array(k_rows, B * H * N)
+    out = {n: np.zeros((len(qr), d)) for n in ("dq", "mag_dq")}
+    out.update({n: np.zeros((len(kr), d)) for n in ("dk", "dv", "mag_dk", "mag_dv")})
+    used = _load().oracle_attention_backward(
+        _ptr(qb), _ptr(kb), _ptr(vb), _ptr(od), _ptr(dod), _ptr(ld), B, H, N, d, int(bool(causal)), float(scale),
+        _ptr(qr), len(qr), _ptr(kr), len(kr), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+        _ptr(out["mag_dq"]), _ptr(out["mag_dk"]), _ptr(out["mag_dv"]), int(n_threads))
+    if used < 0:
+        raise ValueError(f"oracle rejected the arguments (code {used})")
+    return out
 
 
 def attention_online(q, k, v, causal: bool, scale: float, tile: int = 128, rows=None, mutation: int = MUT_NONE,

@@ -34,6 +34,10 @@
  *    row, and does not").  A tile of 1 is the scalar recurrence of the
  *    infra-guide page, section 2.1.
  *
+ *  - oracle_attention_backward: gradients dQ, dK, dV of L = sum(O * dO),
+ *    the scores recomputed from Q and K and normalised with the saved LSE
+ *    ("Online Softmax: Tiling Across a Reduction", backward-pass section).
+ *
  *  - oracle_attention_masked: the three-pass route over the keys a general
  *    mask leaves visible -- a window of keys around the query and, when
  *    document ids are given, only keys of the query's own document (the
@@ -376,4 +380,142 @@ int oracle_attention_masked(const uint16_t* q, const uint16_t* k, const uint16_t
     jb.rows = rows; jb.n_rows = n_rows; jb.o = o; jb.lse = lse; jb.route = 2;
     jb.H = H; jb.window_left = window_left; jb.window_right = window_right; jb.doc = doc;
     return run(&jb, n_threads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass: gradients of L = sum(O * dO) through O = softmax(S) V,     */
+/* S = scale Q K^T, with the scores recomputed from Q and K and normalised   */
+/* by the saved per-row statistic LSE (the recomputation of "Online Softmax: */
+/* Tiling Across a Reduction", backward-pass section).  For visible pairs:  */
+/*   P_ij = exp(S_ij - LSE_i),  D_i = sum_c dO_ic O_ic,                       */
+/*   dV_j = sum_i P_ij dO_i,    dS_ij = P_ij (dO_i . v_j - D_i),              */
+/*   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i.            */
+/* mag_* hold the same sums over absolute values of every term (the         */
+/* conditioning of each element, used for error bounds).                    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    const double *o, *dout, *lse;
+    int64_t N, d;
+    int causal;
+    double scale;
+    const int64_t *q_rows, *k_rows;
+    int64_t n_q, n_k;
+    double *dq, *dk, *dv, *mdq, *mdk, *mdv;
+    int64_t next;
+    pthread_mutex_t lock;
+} bwd_job_t;
+
+static double row_D(const double* dout_row, const double* o_row, int64_t d) {
+    double acc = 0.0;
+    for (int64_t c = 0; c < d; ++c) acc += dout_row[c] * o_row[c];
+    return acc;
+}
+
+static double dot_bd(const double* x, const uint16_t* y, int64_t d) {
+    double acc = 0.0;
+    for (int64_t c = 0; c < d; ++c) acc += x[c] * bf16_bits_to_double(y[c]);
+    return acc;
+}
+
+/* one query row: dQ_i */
+static void bwd_query_row(const bwd_job_t* jb, int64_t flat, double* dq, double* mdq) {
+    const int64_t N = jb->N, d = jb->d;
+    const int64_t bh = flat / N, i = flat % N;
+    const uint16_t* qrow = jb->q + flat * d;
+    const uint16_t* kh = jb->k + bh * N * d;
+    const uint16_t* vh = jb->v + bh * N * d;
+    const double* dor = jb->dout + flat * d;
+    const double Di = row_D(dor, jb->o + flat * d, d);
+    const double Li = jb->lse[flat];
+    for (int64_t c = 0; c < d; ++c) dq[c] = mdq[c] = 0.0;
+    const int64_t nvis = visible_keys(i, N, jb->causal);
+    for (int64_t j = 0; j < nvis; ++j) {
+        const double p = exp(score(qrow, kh + j * d, d, jb->scale) - Li);
+        const double ds = p * (dot_bd(dor, vh + j * d, d) - Di);
+        for (int64_t c = 0; c < d; ++c) {
+            const double kc = bf16_bits_to_double(kh[j * d + c]);
+            dq[c] += jb->scale * ds * kc;
+            mdq[c] += jb->scale * fabs(ds) * fabs(kc);
+        }
+    }
+}
+
+/* one key row: dK_j and dV_j */
+static void bwd_key_row(const bwd_job_t* jb, int64_t flat, double* dk, double* dv, double* mdk, double* mdv) {
+    const int64_t N = jb->N, d = jb->d;
+    const int64_t bh = flat / N, j = flat % N;
+    const uint16_t* krow = jb->k + flat * d;
+    const uint16_t* vrow = jb->v + flat * d;
+    for (int64_t c = 0; c < d; ++c) dk[c] = dv[c] = mdk[c] = mdv[c] = 0.0;
+    for (int64_t i = jb->causal ? j : 0; i < N; ++i) {
+        const int64_t qf = bh * N + i;
+        const uint16_t* qrow = jb->q + qf * d;
+        const double* dor = jb->dout + qf * d;
+        const double p = exp(score(qrow, krow, d, jb->scale) - jb->lse[qf]);
+        const double ds = p * (dot_bd(dor, vrow, d) - row_D(dor, jb->o + qf * d, d));
+        for (int64_t c = 0; c < d; ++c) {
+            const double qc = bf16_bits_to_double(qrow[c]);
+            dv[c] += p * dor[c];
+            mdv[c] += p * fabs(dor[c]);
+            dk[c] += jb->scale * ds * qc;
+            mdk[c] += jb->scale * fabs(ds) * fabs(qc);
+        }
+    }
+}
+
+static void* bwd_worker(void* arg) {
+    bwd_job_t* jb = (bwd_job_t*)arg;
+    for (;;) {
+        pthread_mutex_lock(&jb->lock);
+        int64_t r = jb->next++;
+        pthread_mutex_unlock(&jb->lock);
+        if (r >= jb->n_q + jb->n_k) break;
+        if (r < jb->n_q) {
+            bwd_query_row(jb, jb->q_rows[r], jb->dq + r * jb->d, jb->mdq + r * jb->d);
+        } else {
+            const int64_t s = r - jb->n_q;
+            bwd_key_row(jb, jb->k_rows[s], jb->dk + s * jb->d, jb->dv + s * jb->d, jb->mdk + s * jb->d,
+                        jb->mdv + s * jb->d);
+        }
+    }
+    return NULL;
+}
+
+/* Returns the number of threads used, or a negative value on bad input. */
+int oracle_attention_backward(const uint16_t* q, const uint16_t* k, const uint16_t* v, const double* o,
+                              const double* dout, const double* lse, int64_t B, int64_t H, int64_t N, int64_t d,
+                              int causal, double scale, const int64_t* q_rows, int64_t n_q, const int64_t* k_rows,
+                              int64_t n_k, double* dq, double* dk, double* dv, double* mag_dq, double* mag_dk,
+                              double* mag_dv, int n_threads) {
+    if (!q || !k || !v || !o || !dout || !lse || B < 1 || H < 1 || N < 1 || d < 1) return -1;
+    if ((n_q > 0 && (!q_rows || !dq || !mag_dq)) || (n_k > 0 && (!k_rows || !dk || !dv || !mag_dk || !mag_dv)))
+        return -1;
+    for (int64_t r = 0; r < n_q; ++r)
+        if (q_rows[r] < 0 || q_rows[r] >= B * H * N) return -2;
+    for (int64_t r = 0; r < n_k; ++r)
+        if (k_rows[r] < 0 || k_rows[r] >= B * H * N) return -2;
+    bwd_job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.k = k; jb.v = v; jb.o = o; jb.dout = dout; jb.lse = lse;
+    jb.N = N; jb.d = d; jb.causal = causal; jb.scale = scale;
+    jb.q_rows = q_rows; jb.k_rows = k_rows; jb.n_q = n_q; jb.n_k = n_k;
+    jb.dq = dq; jb.dk = dk; jb.dv = dv; jb.mdq = mag_dq; jb.mdk = mag_dk; jb.mdv = mag_dv;
+    if (n_threads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        n_threads = n > 0 ? (int)n : 1;
+    }
+    if (n_threads > 256) n_threads = 256;
+    const int64_t work = n_q + n_k;
+    if ((int64_t)n_threads > work) n_threads = work > 0 ? (int)work : 1;
+    pthread_mutex_init(&jb.lock, NULL);
+    pthread_t th[256];
+    int started = 0;
+    for (int t = 0; t < n_threads; ++t)
+        if (pthread_create(&th[t], NULL, bwd_worker, &jb) == 0) ++started;
+    if (started == 0) bwd_worker(&jb);
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    pthread_mutex_destroy(&jb.lock);
+    return started > 0 ? started : 1;
 }

@@ -438,3 +438,52 @@ def test_masks_brute_force_tiny():
         o, lse = oracle.attention_masked(q, k, v, 0.125, wl, wr, doc if use_doc else None)
         assert np.max(np.abs(o - O)) <= 1e-12, (wl, wr, use_doc)
         assert np.max(np.abs(lse - L)) <= 1e-12, (wl, wr, use_doc)
+
+
+# --------------------------------------------------------------------------
+# backward pass: gradients of L = sum(O * dO), scores recomputed and
+# normalised with the saved LSE ("Online Softmax: Tiling Across a Reduction",
+# backward-pass section); pinned to automatic differentiation in float64
+# --------------------------------------------------------------------------
+
+def autograd_reference(q, k, v, dout, causal, scale):
+    qd, kd, vd = (t.double().clone().requires_grad_(True) for t in (q, k, v))
+    S = torch.einsum("bhid,bhjd->bhij", qd, kd) * scale
+    N = S.shape[-1]
+    if causal:
+        S = S.masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), float("-inf"))
+    lse = torch.logsumexp(S, dim=-1)
+    O = torch.einsum("bhij,bhjd->bhid", torch.exp(S - lse[..., None]), vd)
+    (O * dout.double()).sum().backward()
+    return O.detach(), lse.detach(), qd.grad, kd.grad, vd.grad
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 1, 64), (2, 2, 50, 64), (1, 2, 130, 128)])
+def test_backward_matches_autograd_float64(causal, B, H, N, d):
+    q, k, v = rand_qkv(B, H, N, d, seed=N + d, std=1.3)
+    dout = bf16(np.random.default_rng(N).standard_normal((B, H, N, d)))
+    scale = 1 / math.sqrt(d)
+    O, lse, gq, gk, gv = autograd_reference(q, k, v, dout, causal, scale)
+    g = oracle.attention_backward(q, k, v, O, dout, lse, causal, scale)
+    for name, ref in (("dq", gq), ("dk", gk), ("dv", gv)):
+        ref = ref.numpy().reshape(-1, d)
+        assert np.max(np.abs(g[name] - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref))), name
+        assert np.all(g["mag_" + name] + 1e-15 >= np.abs(g[name])), name
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_dv_sums_to_dout_and_rows_agree(causal):
+    """Each row's visible weights sum to one, so sum_j dV_j = sum_i dO_i; and a
+    sample of rows equals the same rows of the full computation."""
+    B, H, N, d = 1, 2, 90, 64
+    q, k, v = rand_qkv(B, H, N, d, seed=3)
+    dout = bf16(np.random.default_rng(4).standard_normal((B, H, N, d)))
+    O, lse, *_ = autograd_reference(q, k, v, dout, causal, 0.125)
+    g = oracle.attention_backward(q, k, v, O, dout, lse, causal, 0.125)
+    dv = g["dv"].reshape(B, H, N, d).sum(axis=2)
+    assert np.max(np.abs(dv - as_f64(dout).sum(axis=2))) <= 1e-11
+    rows = np.array([0, 5, 89, 90, 133, 179])
+    gs = oracle.attention_backward(q, k, v, O, dout, lse, causal, 0.125, q_rows=rows, k_rows=rows[::-1])
+    assert np.array_equal(gs["dq"], g["dq"][rows])
+    assert np.array_equal(gs["dk"], g["dk"][rows[::-1]]) and np.array_equal(gs["dv"], g["dv"][rows[::-1]])
