@@ -193,6 +193,40 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 int fa_splitkv_auto_splits(int B, int H, int N, int d, int causal);
 
 /*
+ * fa_bwd -- attention backward pass: the gradients of L = sum(O * dO) with
+ * respect to q, k and v, for the forward of fa_fwd.  Nothing of the N x N
+ * weights is read back: the scores are recomputed tile by tile from q and k
+ * and normalised with the saved per-row statistic lse, so every tile is
+ * final in one pass ("Online Softmax: Tiling Across a Reduction",
+ * backward-pass section).  With P = exp(scale q k^T - lse) and
+ * D_i = sum_c dO_ic o_ic (visible pairs only):
+ *
+ *     dv = P^T dO,   ds = P * (dO v^T - D),   dq = scale ds k,   dk = scale ds^T q
+ *
+ *   q, k, v    : device bf16 [B][H][N][d], the forward's inputs.
+ *   o, lse     : device bf16 [B][H][N][d] and fp32 [B][H][N], the forward's
+ *                outputs (lse is the natural-log statistic fa_fwd writes).
+ *   dout       : device bf16 [B][H][N][d], the gradient of L with respect to o.
+ *   dq, dk, dv : device bf16 [B][H][N][d], written.
+ *   causal, scale, B, H, N, d : as fa_fwd.
+ *   workspace  : device memory owned by the caller, 4-byte aligned, at least
+ *                fa_bwd_workspace_bytes() bytes (D, fp32 per row); contents on
+ *                entry do not matter.
+ *
+ * Bf16 tensors 16-byte aligned; outputs and workspace must not overlap any
+ * input or each other.  Three kernels are enqueued on `stream` (D, then dq,
+ * then dk and dv).  Returns FA_OK, or FA_ERR_NULL_POINTER, FA_ERR_HEAD_DIM,
+ * FA_ERR_SHAPE, FA_ERR_ALIGNMENT, FA_ERR_SCALE, FA_ERR_WORKSPACE,
+ * FA_ERR_ALIAS, FA_ERR_DEVICE, FA_ERR_TENSOR_MAP, FA_ERR_CUDA.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* workspace,
+           size_t workspace_bytes, fa_stream_t stream);
+
+/* Workspace bytes fa_bwd needs: B*H*N*4; 0 for invalid arguments. */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * fa_softmax_rows -- row-wise softmax of an fp32 matrix with the online
  * normaliser ("5.2 CUDA Online Softmax", sections 2 and 4.1; "Online softmax,
  * and the register that can't move", section "Online softmax"):

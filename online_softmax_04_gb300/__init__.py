@@ -79,6 +79,10 @@ def lib() -> ctypes.CDLL:
             L.fa_watchdog_selftest.restype = I
             L.fa_softmax_rows.argtypes = [P, P, P, ctypes.c_longlong, I, P]
             L.fa_softmax_rows.restype = I
+            L.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, ctypes.c_size_t, P]
+            L.fa_bwd.restype = I
+            L.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
+            L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
             L.fa_version.argtypes = []
             L.fa_version.restype = I
             _lib = L
@@ -235,6 +239,32 @@ def softmax(x, stream=None, out=None, with_lse: bool = True):
     lse = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if with_lse else None
     fa_softmax_rows(x, y, lse, M, N, stream)
     return y, lse
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int, causal: bool, scale: float, workspace,
+           workspace_bytes: int, stream=None) -> None:
+    """Enqueue the backward pass; raises FaError on a nonzero C return code."""
+    rc = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                      int(B), int(H), int(N), int(d), 1 if causal else 0, float(scale), _ptr(workspace),
+                      int(workspace_bytes), _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(int(B), int(H), int(N), int(d)))
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, stream=None):
+    """Gradients (dq, dk, dv), bf16 like q, for the forward outputs o, lse and the gradient dout."""
+    import torch
+
+    B, H, N, d = q.shape
+    ws = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, (1.0 / math.sqrt(d)) if scale is None else scale,
+           ws, ws.numel(), stream)
+    return dq, dk, dv
 
 
 def fa_get_device_status() -> int:

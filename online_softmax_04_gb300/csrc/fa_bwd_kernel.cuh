@@ -1,0 +1,527 @@
+// fa_bwd_kernel.cuh -- attention backward pass for sm_103a (GB300).
+//
+// Gradients of L = sum(O * dO) through O = softmax(scale Q K^T) V.  Nothing of
+// the forward's N x N weights is stored: the scores are recomputed tile by
+// tile from Q and K and normalised with the saved per-row statistic LSE, so
+// each tile is final in one pass -- no running max or rescaling on the way
+// back ("Online Softmax: Tiling Across a Reduction", backward-pass section).
+// For a visible pair (i, j):
+//
+//     P_ij  = exp(S_ij - LSE_i)                     S_ij = scale q_i . k_j
+//     D_i   = sum_c dO_ic O_ic
+//     dV_j  = sum_i P_ij dO_i
+//     dS_ij = P_ij (dO_i . v_j - D_i)
+//     dQ_i  = scale sum_j dS_ij k_j,      dK_j = scale sum_i dS_ij q_i
+//
+// Three kernels, enqueued in this order:
+//   * fa_bwd_delta: D_i, one warp per row, into a caller workspace.
+//   * fa_bwd_dq_sm103: one CTA per query tile (Q, dO resident in shared
+//     memory; K_j, V_j streamed by TMA).  Per key tile: S = Q K_j^T and
+//     dP = dO V_j^T on tcgen05.mma into TMEM; the four compute warps (thread =
+//     query row = TMEM lane) turn them into dS in bf16, written back to TMEM;
+//     dQ += dS K_j is a TMEM-A (TS) product.  dQ never leaves TMEM until the
+//     epilogue, so no atomics are needed.
+//   * fa_bwd_dkdv_sm103: one CTA per key tile (K, V resident; Q_i, dO_i
+//     streamed).  Per query tile: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM;
+//     the compute warps (thread = key row) write P^T and dS^T in bf16 over the
+//     columns they have just read; dV += P^T dO_i and dK += dS^T Q_i are TS
+//     products accumulating in TMEM.
+// Splitting dQ from dK/dV costs two extra products per tile pair (S and dP
+// are formed twice) and buys kernels with no cross-CTA reduction.
+//
+// Warp roles (256 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs, warps 4-7 compute.  Every barrier wait is bounded by the
+// same watchdog as the forward kernel.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+constexpr int kBwdThreads = 256;
+
+// D_i = sum_c dO_ic O_ic in fp32, one warp per row; rows = B*H*N
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_bwd_delta(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
+                 long long rows) {
+    const long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(o + (size_t)row * D);
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(dout + (size_t)row * D);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = lane; c < D / 2; c += 32) {
+        const float2 a = __bfloat1622float2(o2[c]), b = __bfloat1622float2(d2[c]);
+        acc = fmaf(a.x, b.x, acc);
+        acc = fmaf(a.y, b.y, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) delta[row] = acc;
+}
+
+struct BwdParams {
+    void* grad;             // dq kernel: dQ; dkdv kernel: dK (bf16 [B*H][N][d])
+    void* grad2;            // dkdv kernel: dV
+    const float* lse;       // fp32 [B*H][N], natural log
+    const float* delta;     // fp32 [B*H][N]
+    int N, n_tiles, causal;
+    float scale, scale_log2;
+    unsigned long long watchdog_ns;
+};
+
+// shared memory of the backward kernels: two resident tiles, a ring of NS
+// stages of two streamed tiles, barriers, per-warp LSE/D staging
+template <int D, int NS>
+struct BwdSmem {
+    static constexpr int kChunks = D / 64;
+    static constexpr uint32_t kTileBytes = 128u * D * 2u;
+    static constexpr uint32_t kOffRes = 0;                            // resident tiles A, B
+    static constexpr uint32_t kOffRing = 2 * kTileBytes;              // [NS][2] streamed tiles
+    static constexpr uint32_t kOffBar = kOffRing + NS * 2 * kTileBytes;
+    static constexpr int kBarRes = 0;                   // resident tiles landed
+    static constexpr int kBarFull = 1;                  // [NS] stage landed
+    static constexpr int kBarEmpty = kBarFull + NS;     // [NS] stage consumed by the MMAs
+    static constexpr int kBarSFull = kBarEmpty + NS;    // the two score-like products of a step finished
+    static constexpr int kBarDSFull = kBarSFull + 1;    // compute warps wrote the bf16 operand(s)
+    static constexpr int kBarUsed = kBarDSFull + 1;     // the products reading those operands finished
+    static constexpr int kBarFinal = kBarUsed + 1;      // the accumulators are complete
+    static constexpr int kBarDrain = kBarFinal + 1;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr uint32_t kOffStage = kOffBar + kNumBars * 8;     // [4 warps][2][LSE 128, D 128] floats
+    static constexpr uint32_t kOffTmemSlot = kOffStage + 4 * 2 * 256 * 4;
+    static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+    static constexpr uint32_t kBytes = kOffAbort + 4;
+    static constexpr uint32_t kAlloc = kBytes + 1024;
+    static_assert(kAlloc <= 232448u, "shared memory");
+};
+
+// loads of the 64-column chunks of a [128 rows][D] tile
+template <int D>
+__device__ __forceinline__ void bwd_load_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row0, int bh) {
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * kChunkBytes, m, bar, c * 64, row0, bh);
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per (query tile, head).  TMEM: S [0,128), dP [128,256),
+// dQ [256, 256+D), dS bf16 [256+D, 256+D+64).
+// ---------------------------------------------------------------------------
+template <int D, int NS>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dq_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+    using L = BwdSmem<D, NS>;
+    constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+    auto bar = [&](int i) -> uint32_t { return sbase + L::kOffBar + 8u * (uint32_t)i; };
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+    const int lane = (int)(threadIdx.x & 31);
+    const uint64_t limit = p.watchdog_ns;
+    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest causal tiles first
+    const int bh = (int)blockIdx.y;
+    const int n_kv = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;
+
+    if (warp == 0 && lane == 0) {
+        mbar_init(bar(L::kBarRes), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(L::kBarFull + s), 1);
+            mbar_init(bar(L::kBarEmpty + s), 1);
+        }
+        mbar_init(bar(L::kBarSFull), 1);
+        mbar_init(bar(L::kBarDSFull), 4);
+        mbar_init(bar(L::kBarUsed), 1);
+        mbar_init(bar(L::kBarFinal), 1);
+        mbar_init(bar(L::kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_do);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t res_q = sbase + L::kOffRes, res_do = sbase + L::kOffRes + L::kTileBytes;
+    auto ring_k = [&](int s) { return sbase + L::kOffRing + (uint32_t)(2 * s) * L::kTileBytes; };
+    auto ring_v = [&](int s) { return sbase + L::kOffRing + (uint32_t)(2 * s + 1) * L::kTileBytes; };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
+            bwd_load_tile<D>(res_q, &tm_q, bar(L::kBarRes), qt * 128, bh);
+            bwd_load_tile<D>(res_do, &tm_do, bar(L::kBarRes), qt * 128, bh);
+            int j = 0;
+            for (; ok && j < n_kv; ++j) {
+                const int s = j % NS;
+                if (j >= NS)
+                    ok = fa_wait(bar(L::kBarEmpty + s), (uint32_t)(((j - NS) / NS) & 1), abort_flag, limit,
+                                 kStatusLoadWait);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
+                bwd_load_tile<D>(ring_k(s), &tm_k, bar(L::kBarFull + s), j * 128, bh);
+                bwd_load_tile<D>(ring_v(s), &tm_v, bar(L::kBarFull + s), j * 128, bh);
+            }
+            if (!ok || *abort_flag) {  // let every issued copy land before the CTA exits
+                fa_wait_drain(bar(L::kBarRes), 0, limit);
+                for (int s = 0; s < NS; ++s)
+                    if (j > s) fa_wait_drain(bar(L::kBarFull + s), (uint32_t)(((j - 1 - s) / NS) & 1), limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+            constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, false, true);
+            bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
+            auto issue_dq = [&](int jj) {  // dQ += dS K_jj once dS(jj) is in TMEM
+                const int s = jj % NS;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColDQ, tmem + kColDS + (uint32_t)kk * 8u,
+                           sdesc_sw128(ring_k(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescDQ,
+                           (jj > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar(L::kBarEmpty + s));
+                tc_commit(bar(L::kBarUsed));
+            };
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int s = j % NS;
+                ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
+                // S and dP of step j-1 have been read and dS(j-1) written: dQ for j-1,
+                // then the next score products into the same columns
+                if (ok && j > 0)
+                    ok = fa_wait(bar(L::kBarDSFull), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
+                if (!ok) break;
+                if (j > 0) issue_dq(j - 1);
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(tmem + kColS, sdesc_sw128(res_q + off, 16, 1024), sdesc_sw128(ring_k(s) + off, 16, 1024),
+                           kIdescS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(tmem + kColDP, sdesc_sw128(res_do + off, 16, 1024),
+                           sdesc_sw128(ring_v(s) + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(L::kBarSFull));
+            }
+            if (ok && n_kv > 0) {
+                ok = fa_wait(bar(L::kBarDSFull), (uint32_t)((n_kv - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
+                if (ok) {
+                    issue_dq(n_kv - 1);
+                    tc_commit(bar(L::kBarFinal));
+                }
+            }
+            tc_commit(bar(L::kBarDrain));
+            fa_wait_drain(bar(L::kBarDrain), 0, limit);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int q_idx = qt * 128 + row;
+        const bool valid = q_idx < p.N;
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const size_t r = (size_t)bh * p.N + (size_t)q_idx;
+        // rows past N: P = 0 (LSE = +inf), nothing stored
+        const float lse2 = valid ? p.lse[r] * kLog2e : INFINITY;
+        const float drow = valid ? p.delta[r] : 0.f;
+        const float c2 = p.scale_log2;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            ok = fa_wait_warp(bar(L::kBarSFull), (uint32_t)(j & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            // dS(j-1) must have been read by its dQ product before it is overwritten
+            if (ok && j > 0)
+                ok = fa_wait_warp(bar(L::kBarUsed), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusSoftmaxWaitPV);
+            if (!ok) break;
+            tc_fence_after_sync();
+            // keys visible to this row in this tile: c <= last
+            int last = p.N - 1 - j * 128;
+            if (p.causal && j == qt) last = min(last, row);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t sv[32], dv[32], pk[16];
+                tmem_ld32_wait(t_lane + kColS + 32u * ch, sv);
+                tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c0 = 32 * ch + 2 * i;
+                    const float p0 = (c0 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c2, -lse2)) : 0.f;
+                    const float p1 = (c0 + 1 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c2, -lse2)) : 0.f;
+                    pk[i] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * i]) - drow),
+                                        p1 * (__uint_as_float(dv[2 * i + 1]) - drow));
+                }
+                tmem_st16(t_lane + kColDS + 16u * ch, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarDSFull));
+        }
+        if (ok && n_kv > 0) ok = fa_wait_warp(bar(L::kBarFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
+        if (ok) {
+            tc_fence_after_sync();
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.grad) + r * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32_wait(t_lane + kColDQ + 32u * c, v);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack_bf16x2(n_kv > 0 ? __uint_as_float(v[2 * i]) * p.scale : 0.f,
+                                       n_kv > 0 ? __uint_as_float(v[2 * i + 1]) * p.scale : 0.f);
+                if (valid) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) dst[c * 4 + u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                }
+            }
+        }
+        __syncwarp();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: one CTA per (key tile, head).  TMEM: S^T [0,128) (P^T bf16 over its
+// first 64 columns), dP^T [128,256) (dS^T bf16 over its first 64 columns),
+// dV [256, 256+D), dK [256+D, 256+2D).
+// ---------------------------------------------------------------------------
+template <int D, int NS>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dkdv_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const BwdParams p) {
+    using L = BwdSmem<D, NS>;
+    constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+    auto bar = [&](int i) -> uint32_t { return sbase + L::kOffBar + 8u * (uint32_t)i; };
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+    const int lane = (int)(threadIdx.x & 31);
+    const uint64_t limit = p.watchdog_ns;
+    const int kt = (int)blockIdx.x;  // causal: the lowest key tiles see the most query tiles and go first
+    const int bh = (int)blockIdx.y;
+    const int i0 = p.causal ? kt : 0;
+    const int n_q = p.n_tiles - i0;
+
+    if (warp == 0 && lane == 0) {
+        mbar_init(bar(L::kBarRes), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(L::kBarFull + s), 1);
+            mbar_init(bar(L::kBarEmpty + s), 1);
+        }
+        mbar_init(bar(L::kBarSFull), 1);
+        mbar_init(bar(L::kBarDSFull), 4);
+        mbar_init(bar(L::kBarUsed), 1);
+        mbar_init(bar(L::kBarFinal), 1);
+        mbar_init(bar(L::kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_do);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t res_k = sbase + L::kOffRes, res_v = sbase + L::kOffRes + L::kTileBytes;
+    auto ring_q = [&](int s) { return sbase + L::kOffRing + (uint32_t)(2 * s) * L::kTileBytes; };
+    auto ring_do = [&](int s) { return sbase + L::kOffRing + (uint32_t)(2 * s + 1) * L::kTileBytes; };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
+            bwd_load_tile<D>(res_k, &tm_k, bar(L::kBarRes), kt * 128, bh);
+            bwd_load_tile<D>(res_v, &tm_v, bar(L::kBarRes), kt * 128, bh);
+            int i = 0;
+            for (; ok && i < n_q; ++i) {
+                const int s = i % NS;
+                if (i >= NS)
+                    ok = fa_wait(bar(L::kBarEmpty + s), (uint32_t)(((i - NS) / NS) & 1), abort_flag, limit,
+                                 kStatusLoadWait);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
+                bwd_load_tile<D>(ring_q(s), &tm_q, bar(L::kBarFull + s), (i0 + i) * 128, bh);
+                bwd_load_tile<D>(ring_do(s), &tm_do, bar(L::kBarFull + s), (i0 + i) * 128, bh);
+            }
+            if (!ok || *abort_flag) {
+                fa_wait_drain(bar(L::kBarRes), 0, limit);
+                for (int s = 0; s < NS; ++s)
+                    if (i > s) fa_wait_drain(bar(L::kBarFull + s), (uint32_t)(((i - 1 - s) / NS) & 1), limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+            constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);
+            bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
+            for (int i = 0; ok && i < n_q; ++i) {
+                const int s = i % NS;
+                ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((i / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
+                // the columns of S^T and dP^T hold P^T and dS^T of step i-1 until its
+                // dV and dK products have finished
+                if (ok && i > 0)
+                    ok = fa_wait(bar(L::kBarUsed), (uint32_t)((i - 1) & 1), abort_flag, limit, kStatusMmaWaitSFree);
+                if (!ok) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(tmem + kColS, sdesc_sw128(res_k + off, 16, 1024), sdesc_sw128(ring_q(s) + off, 16, 1024),
+                           kIdescS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(tmem + kColDP, sdesc_sw128(res_v + off, 16, 1024),
+                           sdesc_sw128(ring_do(s) + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(L::kBarSFull));
+                ok = fa_wait(bar(L::kBarDSFull), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
+                if (!ok) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_ts(tmem + kColDV, tmem + kColS + (uint32_t)kk * 8u,
+                           sdesc_sw128(ring_do(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescG,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    mma_ts(tmem + kColDK, tmem + kColDP + (uint32_t)kk * 8u,
+                           sdesc_sw128(ring_q(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescG,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(L::kBarEmpty + s));
+                tc_commit(bar(L::kBarUsed));
+            }
+            if (ok && n_q > 0) tc_commit(bar(L::kBarFinal));
+            tc_commit(bar(L::kBarDrain));
+            fa_wait_drain(bar(L::kBarDrain), 0, limit);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // key row of this thread
+        const int k_idx = kt * 128 + row;
+        const bool valid = k_idx < p.N;
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        float* stage = reinterpret_cast<float*>(smem + L::kOffStage) + quarter * 2 * 256;  // [2][LSE 128, D 128]
+        const float c2 = p.scale_log2;
+        bool ok = true;
+        for (int i = 0; i < n_q; ++i) {
+            const int qi = i0 + i;
+            // this query tile's LSE (log2 units) and D, staged once per warp; queries
+            // past N get LSE = +inf, so their weights are 0
+            float* st = stage + (i & 1) * 256;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = u * 32 + lane;
+                const int q = qi * 128 + c;
+                const size_t r = (size_t)bh * p.N + (size_t)q;
+                st[c] = q < p.N ? p.lse[r] * kLog2e : INFINITY;
+                st[128 + c] = q < p.N ? p.delta[r] : 0.f;
+            }
+            __syncwarp();
+            ok = fa_wait_warp(bar(L::kBarSFull), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            if (!ok) break;
+            tc_fence_after_sync();
+            // causal: query q sees key k_idx iff k_idx <= q, i.e. column c >= first
+            const int first = (p.causal && qi == kt) ? row : 0;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t sv[32], dv[32], pk[16], dk[16];
+                tmem_ld32_wait(t_lane + kColS + 32u * ch, sv);
+                tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    const int c0 = 32 * ch + 2 * i2;
+                    const float p0 = (c0 >= first) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i2]), c2, -st[c0])) : 0.f;
+                    const float p1 =
+                        (c0 + 1 >= first) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i2 + 1]), c2, -st[c0 + 1])) : 0.f;
+                    pk[i2] = pack_bf16x2(p0, p1);
+                    dk[i2] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * i2]) - st[128 + c0]),
+                                         p1 * (__uint_as_float(dv[2 * i2 + 1]) - st[128 + c0 + 1]));
+                }
+                // P^T and dS^T over columns already read (16 ch + 16 <= 32 ch + 32)
+                tmem_st16(t_lane + kColS + 16u * ch, pk);
+                tmem_st16(t_lane + kColDP + 16u * ch, dk);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarDSFull));
+        }
+        if (ok && n_q > 0) ok = fa_wait_warp(bar(L::kBarFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
+        if (ok) {
+            tc_fence_after_sync();
+            const size_t r = (size_t)bh * p.N + (size_t)k_idx;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (times scale)
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? p.grad : p.grad2) + r * D);
+                const float f = which ? p.scale : 1.f;
+                const uint32_t col = which ? kColDK : kColDV;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32_wait(t_lane + col + 32u * c, v);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        w[u] = pack_bf16x2(n_q > 0 ? __uint_as_float(v[2 * u]) * f : 0.f,
+                                           n_q > 0 ? __uint_as_float(v[2 * u + 1]) * f : 0.f);
+                    if (valid) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) dst[c * 4 + u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace fa

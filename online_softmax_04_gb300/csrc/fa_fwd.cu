@@ -13,6 +13,7 @@
 #include "../../include/fa.h"
 #include "fa_fwd_kernel.cuh"
 #include "softmax_rows.cuh"
+#include "fa_bwd_kernel.cuh"
 
 namespace {
 
@@ -238,6 +239,30 @@ int queue_slot(unsigned int** out) {
     return FA_OK;
 }
 
+template <int D, int NS>
+int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+               const void* o, const void* dout, float* delta, void* dq, void* dk, void* dv, fa::BwdParams p, int BH,
+               cudaStream_t st) {
+    using L = fa::BwdSmem<D, NS>;
+    const long long rows = (long long)BH * p.N;
+    fa::fa_bwd_delta<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
+                                                                      static_cast<const __nv_bfloat16*>(dout), delta,
+                                                                      rows);
+    auto kq = fa::fa_bwd_dq_sm103<D, NS>;
+    auto kkv = fa::fa_bwd_dkdv_sm103<D, NS>;
+    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess ||
+        cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
+        return FA_ERR_CUDA;
+    const dim3 grid((unsigned)p.n_tiles, (unsigned)BH);
+    p.delta = delta;
+    p.grad = dq;
+    kq<<<grid, fa::kBwdThreads, L::kAlloc, st>>>(tq, tk, tv, tdo, p);
+    p.grad = dk;
+    p.grad2 = dv;
+    kkv<<<grid, fa::kBwdThreads, L::kAlloc, st>>>(tq, tk, tv, tdo, p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -395,6 +420,60 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
         fa::fa_splitkv_merge<128><<<blocks, 256, 0, s>>>(pr.p.ws_o, pr.p.ws_m, pr.p.ws_lbf, pr.p.ws_l32, ob, lse,
                                                          rows, n_splits);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    return (size_t)B * (size_t)H * (size_t)N * sizeof(float);
+}
+
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, void* workspace,
+           size_t workspace_bytes, fa_stream_t stream) {
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_NULL_POINTER;
+    if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+    const long long BH = (long long)B * (long long)H;
+    if (BH > 65535) return FA_ERR_SHAPE;
+    auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+    if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || mis16(dout) || mis16(dq) || mis16(dk) || mis16(dv) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+        return FA_ERR_ALIGNMENT;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+    if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_WORKSPACE;
+    const size_t tb = (size_t)BH * (size_t)N * (size_t)d * 2u, lb = (size_t)BH * (size_t)N * 4u;
+    const void* ins[6] = {q, k, v, o, dout, lse};
+    const size_t in_bytes[6] = {tb, tb, tb, tb, tb, lb};
+    void* outs[4] = {dq, dk, dv, workspace};
+    const size_t out_bytes[4] = {tb, tb, tb, lb};
+    for (int a = 0; a < 4; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA_ERR_ALIAS;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA_ERR_ALIAS;
+    }
+    const int dev_rc = check_device();
+    if (dev_rc != FA_OK) return dev_rc;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_bhnd(&tq, q, d, N, (int)BH) || !encode_bhnd(&tk, k, d, N, (int)BH) ||
+        !encode_bhnd(&tv, v, d, N, (int)BH) || !encode_bhnd(&tdo, dout, d, N, (int)BH))
+        return FA_ERR_TENSOR_MAP;
+    fa::BwdParams p{};
+    p.lse = lse;
+    p.N = N;
+    p.n_tiles = (N + 127) / 128;
+    p.causal = causal ? 1 : 0;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.44269504088896340736f;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        p.watchdog_ns = g_watchdog_ns;
+    }
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* delta = static_cast<float*>(workspace);
+    if (d == 64) return launch_bwd<64, 4>(tq, tk, tv, tdo, o, dout, delta, dq, dk, dv, p, (int)BH, st);
+    return launch_bwd<128, 2>(tq, tk, tv, tdo, o, dout, delta, dq, dk, dv, p, (int)BH, st);
 }
 
 int fa_softmax_rows(const float* x, float* y, float* lse, long long M, int N, fa_stream_t stream) {

@@ -193,6 +193,15 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]
         : "memory");
 }
 
+// store 16 columns (completion needs tmem_st_wait)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        FA_V8(0), FA_V8(8)
+        : "memory");
+}
+
 // store 64 columns with one instruction (completion needs tmem_st_wait)
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&v)[64]) {
     asm volatile(

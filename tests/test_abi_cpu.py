@@ -83,6 +83,31 @@ def test_masked_host_validation(fa):
         assert m() in (fa.FA_ERR_CUDA, fa.FA_ERR_DEVICE)
 
 
+def test_backward_host_validation(fa):
+    L = fa.lib()
+    q, k, v, o, do = (FAKE + (i << 30) for i in range(5))
+    lse, dq, dk, dv, ws = (FAKE + (i << 30) for i in range(5, 10))
+    nws = fa.fa_bwd_workspace_bytes(2, 3, 100, 64)
+    assert nws == 2 * 3 * 100 * 4 and fa.fa_bwd_workspace_bytes(2, 3, 100, 96) == 0
+
+    def b(**kw):
+        a = dict(q=q, k=k, v=v, o=o, do=do, lse=lse, dq=dq, dk=dk, dv=dv, d=64, ws=ws, wsb=nws, scale=0.125)
+        a.update(kw)
+        return L.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"], 2, 3, 100,
+                        a["d"], 1, a["scale"], a["ws"], a["wsb"], 0)
+
+    assert b(do=0) == fa.FA_ERR_NULL_POINTER
+    assert b(ws=0) == fa.FA_ERR_NULL_POINTER
+    assert b(d=256) == fa.FA_ERR_HEAD_DIM
+    assert b(dk=dk + 8) == fa.FA_ERR_ALIGNMENT
+    assert b(scale=0.0) == fa.FA_ERR_SCALE
+    assert b(wsb=nws - 1) == fa.FA_ERR_WORKSPACE
+    assert b(dq=o + 64) == fa.FA_ERR_ALIAS      # dq over o
+    assert b(ws=dv + 64) == fa.FA_ERR_ALIAS     # workspace over dv
+    if not torch.cuda.is_available():
+        assert b() in (fa.FA_ERR_CUDA, fa.FA_ERR_DEVICE)
+
+
 def test_softmax_rows_host_validation(fa):
     L = fa.lib()
     x, y, lse = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
