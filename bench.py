@@ -367,6 +367,145 @@ def run_softmax(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+BWD_METRIC = "attention backward TFLOP/s (bf16, 1 GB300; 5 products per tile pair counted) and % of dense BF16 peak"
+
+
+def run_backward(args, w, rank, world, local_rank):
+    """One step = one fa_bwd call (D, dQ, dK, dV) on the workload; FLOPs =
+    2.5 x the forward's (five N x N x d products instead of two)."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    if w.masked:
+        raise SystemExit("the backward pass takes full or causal attention")
+    flops = 2.5 * workload_flops(w)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from online_softmax_04_gb300 import workloads as wl
+        import oracle
+
+        q, k, v = wl.make_inputs(w)
+        rng = np.random.default_rng(w.seed + 9)
+        dout = torch.from_numpy(rng.standard_normal(q.shape, dtype=np.float32)).to(torch.bfloat16)
+        o = torch.zeros(q.shape, dtype=torch.float32)   # D_i = 0: the oracle's cost does not depend on O
+        lse = torch.zeros(q.shape[:3], dtype=torch.float32)
+        total = w.B * w.H * w.N
+        n = 64
+        secs, fl = 0.0, 0.0
+        for step in range(args.warmup + args.steps):
+            rows = rng.integers(0, total, n)
+            t0 = time.perf_counter()
+            oracle.attention_backward(q, k, v, o, dout, lse, w.causal, w.scale, q_rows=rows, k_rows=rows)
+            dt = time.perf_counter() - t0
+            if step >= args.warmup:
+                secs += dt
+                fl += 2.5 * row_flops(w, rows)   # the per-row share of the same 10 d per visible pair
+        value = fl / secs / 1e12
+        print(json.dumps({"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": w.name, "op": "backward"},
+                          "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count() or 1,
+                                           "kind": "oracle", "sample": f"{n} query rows and {n} key rows per step"},
+                          "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    if local_rank == 0:
+        __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    import online_softmax_04_gb300 as fa
+    from online_softmax_04_gb300 import workloads as wl
+
+    wr = rank_workload(w, rank)
+    q, k, v = wl.make_inputs(wr)
+    rng = np.random.default_rng(wr.seed + 9)
+    hdo = torch.from_numpy(rng.standard_normal(q.shape, dtype=np.float32)).to(torch.bfloat16)
+    dq_, dk_, dv_, ddo = q.to(dev), k.to(dev), v.to(dev), hdo.to(dev)
+    o, lse = fa.attention(dq_, dk_, dv_, causal=w.causal)     # the forward the backward belongs to
+    gq, gk, gv = torch.empty_like(dq_), torch.empty_like(dk_), torch.empty_like(dv_)
+    ws_bytes = fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_bwd(dq_, dk_, dv_, o, ddo, lse, gq, gk, gv, w.B, w.H, w.N, w.d, w.causal, w.scale, ws, ws_bytes, stream)
+
+    fa.fa_clear_device_status()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    io = 8 * q.numel() * 2
+    flush = L2Flush(torch, dev) if io < 2 * L2_BYTES else None
+
+    def timed(fn, n):
+        torch.cuda.synchronize()
+        if flush is not None:
+            ms = 0.0
+            for _ in range(n):
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ms += e0.elapsed_time(e1)
+            return ms
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    with ClockSampler(local_rank) as clk:
+        ms_total = timed(step, args.steps)
+    ms_step = ms_total / args.steps
+    value = flops / (ms_step * 1e-3) / 1e12
+    host = [t.pin_memory() for t in (q, k, v, o.cpu(), hdo, lse.cpu())]
+    outs_h = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3)]
+    devs = [dq_, dk_, dv_, o, ddo, lse]
+
+    def e2e_step():
+        for hd, dd in zip(host, devs):
+            dd.copy_(hd, non_blocking=True)
+        step()
+        for hd, dd in zip(outs_h, (gq, gk, gv)):
+            hd.copy_(dd, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    ms_e2e = timed(e2e_step, args.steps) / args.steps
+    if fa.fa_get_device_status() != 0:
+        raise SystemExit("a backward kernel gave up on a barrier")
+    if rank != 0:
+        return
+    peak, src = measured_peak()
+    line = {
+        "metric": BWD_METRIC, "value": value * world, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "op": "backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "flops_per_step_per_gpu": flops, "entry_point": "fa_bwd",
+                   "l2": "L2 flushed before each step" if flush is not None else "inputs larger than L2"},
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
+                     "traffic": None, "peak_source": src,
+                     "kernel": "fa_bwd_delta + fa_bwd_dq_sm103 + fa_bwd_dkdv_sm103"},
+        "cpu_baseline": None,
+        "e2e": {"value": flops * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host),
+                "d2h_bytes_per_step": 3 * q.numel() * 2, "ms_per_step": ms_e2e},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, w, rank, world):
     """The oracle as the reference arm: K timed steps, each a bounded row sample."""
     if rank != 0:
@@ -418,8 +557,8 @@ def main():
     ap.add_argument("--splitkv", type=int, default=-1,
                     help="use the split-KV entry point with this many splits (0 = automatic; default: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "softmax"], default="attention",
-                    help="attention (the headline) or the standalone row softmax")
+    ap.add_argument("--op", choices=["attention", "softmax", "backward"], default="attention",
+                    help="attention (the headline forward), the standalone row softmax, or the attention backward")
     ap.add_argument("--rows", type=int, default=4096, help="--op softmax: M")
     ap.add_argument("--cols", type=int, default=4096, help="--op softmax: N")
     args = ap.parse_args()
@@ -439,6 +578,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.op == "backward":
+        run_backward(args, w, rank, world, local_rank)
+        return
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return
