@@ -16,9 +16,9 @@
 //
 // GB300 mapping:
 //   * Persistent grid, one CTA per SM, each working through a sequence of query
-//     tiles: causal tiles paired long with short and dealt out statically for
-//     most of the work, the rest handed out one tile at a time from a global
-//     counter.  The TMA ring, the S/P double buffers and every barrier phase
+//     tiles: causal tiles paired long with short and dealt out statically in
+//     full rounds, the partial last round handed out one tile at a time from a
+//     global counter.  The TMA ring, the S/P double buffers and every barrier phase
 //     run on across tile boundaries, so the loads and first S products of the
 //     next tile overlap the end of this one.
 //   * S_j = Q K_j^T and O += P_j V_j run on tcgen05.mma (bf16 in, fp32
@@ -248,11 +248,12 @@ struct TileWork {
 // a long causal tile with a short one, so that every pair costs about the
 // same; pairs are numbered head-major (the CTAs busy at any moment share the
 // keys and values of a few heads in L2).  Each CTA first takes static_rounds
-// pairs statically (pairs blockIdx.x, blockIdx.x + gridDim.x, ...), which keeps
-// a pair's two tiles, and the shared keys and values, on one SM.  The
-// remaining pairs are split into single tiles that CTAs take one at a time
-// from a global counter -- first all their long tiles, then the short ones --
-// so that CTAs that ran faster (or got less) do more of the tail.
+// pairs statically (pairs blockIdx.x, blockIdx.x + gridDim.x, ...; the host
+// deals out every full round), which keeps a pair's two tiles, and the shared
+// keys and values, on one SM.  The remaining pairs are split into single tiles
+// that CTAs take one at a time from a global counter -- first all their long
+// tiles, then the short ones -- so that CTAs that ran faster do more of the
+// tail.
 __host__ __device__ inline long long persistent_pairs(const FaParams& p) {
     return (long long)p.BH * ((p.n_tiles + 1) / 2);
 }
