@@ -17,7 +17,7 @@
 //   * fa_bwd_delta: D_i, one warp per row, into a caller workspace.
 //   * fa_bwd_dq_sm103: one CTA per query tile (Q, dO resident in shared
 //     memory; K_j, V_j streamed by TMA).  Per key tile: S = Q K_j^T and
-//     dP = dO V_j^T on tcgen05.mma into TMEM; the four compute warps (thread =
+//     dP = dO V_j^T on tcgen05.mma into TMEM; the compute warps (thread =
 //     query row = TMEM lane) turn them into dS in bf16, written back to TMEM;
 //     dQ += dS K_j is a TMEM-A (TS) product.  dQ never leaves TMEM until the
 //     epilogue, so no atomics are needed.
@@ -29,9 +29,10 @@
 // Splitting dQ from dK/dV costs two extra products per tile pair (S and dP
 // are formed twice) and buys kernels with no cross-CTA reduction.
 //
-// Warp roles (256 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs, warps 4-7 compute.  Every barrier wait is bounded by the
-// same watchdog as the forward kernel.
+// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs, warps 4-11 compute: two warps per 32-row TMEM lane quarter,
+// each taking half of the 128 columns of a step and half of the epilogue.
+// Every barrier wait is bounded by the same watchdog as the forward kernel.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -40,7 +41,7 @@
 
 namespace fa {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;  // 12 warps: 8 of them compute, two per TMEM lane quarter
 
 // D_i = sum_c dO_ic O_ic in fp32, one warp per row; rows = B*H*N
 template <int D>
@@ -92,8 +93,8 @@ struct BwdSmem {
     static constexpr int kBarFinal = kBarUsed + 1;      // the accumulators are complete
     static constexpr int kBarDrain = kBarFinal + 1;
     static constexpr int kNumBars = kBarDrain + 1;
-    static constexpr uint32_t kOffStage = kOffBar + kNumBars * 8;     // [4 warps][2][LSE 128, D 128] floats
-    static constexpr uint32_t kOffTmemSlot = kOffStage + 4 * 2 * 256 * 4;
+    static constexpr uint32_t kOffStage = kOffBar + kNumBars * 8;     // [8 warps][2][LSE 128, D 128] floats
+    static constexpr uint32_t kOffTmemSlot = kOffStage + 8 * 2 * 256 * 4;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
     static constexpr uint32_t kBytes = kOffAbort + 4;
     static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar(L::kBarEmpty + s), 1);
         }
         mbar_init(bar(L::kBarSFull), 1);
-        mbar_init(bar(L::kBarDSFull), 4);
+        mbar_init(bar(L::kBarDSFull), 8);
         mbar_init(bar(L::kBarUsed), 1);
         mbar_init(bar(L::kBarFinal), 1);
         mbar_init(bar(L::kBarDrain), 1);
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         const int quarter = warp & 3;
+        const int half = (warp - 4) >> 2;  // columns [64 half, 64 half + 64) of every step
         const int row = quarter * 32 + lane;
         const int q_idx = qt * 128 + row;
         const bool valid = q_idx < p.N;
@@ -259,7 +261,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             int last = p.N - 1 - j * 128;
             if (p.causal && j == qt) last = min(last, row);
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int hc = 0; hc < 2; ++hc) {
+                const int ch = 2 * half + hc;
                 uint32_t sv[32], dv[32], pk[16];
                 tmem_ld32_wait(t_lane + kColS + 32u * ch, sv);
                 tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
@@ -283,7 +286,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after_sync();
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.grad) + r * D);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int hc = 0; hc < D / 64; ++hc) {  // this warp's half of the columns
+                const int c = half * (D / 64) + hc;
                 uint32_t v[32];
                 tmem_ld32_wait(t_lane + kColDQ + 32u * c, v);
                 uint32_t w[16];
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ---------------------------------------------------------------------------
 // dK, dV: one CTA per (key tile, head).  TMEM: S^T [0,128) (P^T bf16 over its
-// first 64 columns), dP^T [128,256) (dS^T bf16 over its first 64 columns),
+// columns [0,32) and [64,96)), dP^T [128,256) (dS^T bf16 likewise),
 // dV [256, 256+D), dK [256+D, 256+2D).
 // ---------------------------------------------------------------------------
 template <int D, int NS>
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar(L::kBarEmpty + s), 1);
         }
         mbar_init(bar(L::kBarSFull), 1);
-        mbar_init(bar(L::kBarDSFull), 4);
+        mbar_init(bar(L::kBarDSFull), 8);
         mbar_init(bar(L::kBarUsed), 1);
         mbar_init(bar(L::kBarFinal), 1);
         mbar_init(bar(L::kBarDrain), 1);
@@ -417,15 +421,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ok = fa_wait(bar(L::kBarDSFull), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
                 if (!ok) break;
                 tc_fence_after_sync();
+                // the bf16 operands of queries 16 kk .. 16 kk + 15 sit at column
+                // 8 kk (first half of the queries) or 32 + 8 kk (second half)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    mma_ts(tmem + kColDV, tmem + kColS + (uint32_t)kk * 8u,
+                    mma_ts(tmem + kColDV, tmem + kColS + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
                            sdesc_sw128(ring_do(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescG,
                            (i > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    mma_ts(tmem + kColDK, tmem + kColDP + (uint32_t)kk * 8u,
+                    mma_ts(tmem + kColDK, tmem + kColDP + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
                            sdesc_sw128(ring_q(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescG,
                            (i > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -439,11 +445,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         const int quarter = warp & 3;
+        const int half = (warp - 4) >> 2;      // query columns [64 half, 64 half + 64) of every step
         const int row = quarter * 32 + lane;  // key row of this thread
         const int k_idx = kt * 128 + row;
         const bool valid = k_idx < p.N;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        float* stage = reinterpret_cast<float*>(smem + L::kOffStage) + quarter * 2 * 256;  // [2][LSE 128, D 128]
+        float* stage = reinterpret_cast<float*>(smem + L::kOffStage) + (warp - 4) * 2 * 256;  // [2][LSE 128, D 128]
         const float c2 = p.scale_log2;
         bool ok = true;
         for (int i = 0; i < n_q; ++i) {
@@ -466,7 +473,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // causal: query q sees key k_idx iff k_idx <= q, i.e. column c >= first
             const int first = (p.causal && qi == kt) ? row : 0;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int hc = 0; hc < 2; ++hc) {
+                const int ch = 2 * half + hc;
                 uint32_t sv[32], dv[32], pk[16], dk[16];
                 tmem_ld32_wait(t_lane + kColS + 32u * ch, sv);
                 tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
@@ -480,9 +488,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     dk[i2] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * i2]) - st[128 + c0]),
                                          p1 * (__uint_as_float(dv[2 * i2 + 1]) - st[128 + c0 + 1]));
                 }
-                // P^T and dS^T over columns already read (16 ch + 16 <= 32 ch + 32)
-                tmem_st16(t_lane + kColS + 16u * ch, pk);
-                tmem_st16(t_lane + kColDP + 16u * ch, dk);
+                // P^T and dS^T of query columns [64 half, +64) go to columns
+                // [64 half, 64 half + 32): inside what this warp has already read
+                // (64 half + 16 hc + 16 <= 64 half + 32 hc + 32), never into the other
+                // half's columns
+                tmem_st16(t_lane + kColS + 64u * half + 16u * hc, pk);
+                tmem_st16(t_lane + kColDP + 64u * half + 16u * hc, dk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -499,7 +510,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const float f = which ? p.scale : 1.f;
                 const uint32_t col = which ? kColDK : kColDV;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int hc = 0; hc < D / 64; ++hc) {  // this warp's half of the columns
+                    const int c = half * (D / 64) + hc;
                     uint32_t v[32];
                     tmem_ld32_wait(t_lane + col + 32u * c, v);
                     uint32_t w[16];
