@@ -92,7 +92,8 @@ struct BwdSmem {
     static constexpr int kBarUsed = kBarDSFull + 1;     // the products reading those operands finished
     static constexpr int kBarFinal = kBarUsed + 1;      // the accumulators are complete
     static constexpr int kBarDrain = kBarFinal + 1;
-    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kBarSRead = kBarDrain + 1;     // dQ kernel: the compute warps hold S and dP in registers
+    static constexpr int kNumBars = kBarSRead + 1;
     static constexpr uint32_t kOffStage = kOffBar + kNumBars * 8;     // [8 warps][2][LSE 128, D 128] floats
     static constexpr uint32_t kOffTmemSlot = kOffStage + 8 * 2 * 256 * 4;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::kBarUsed), 1);
         mbar_init(bar(L::kBarFinal), 1);
         mbar_init(bar(L::kBarDrain), 1);
+        mbar_init(bar(L::kBarSRead), 8);
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_q);
@@ -205,12 +207,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int s = j % NS;
                 ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
-                // S and dP of step j-1 have been read and dS(j-1) written: dQ for j-1,
-                // then the next score products into the same columns
+                // S and dP of step j-1 are in the compute warps' registers: the next
+                // score products may overwrite their columns while dS(j-1) is formed
                 if (ok && j > 0)
-                    ok = fa_wait(bar(L::kBarDSFull), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
+                    ok = fa_wait(bar(L::kBarSRead), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusMmaWaitSFree);
                 if (!ok) break;
-                if (j > 0) issue_dq(j - 1);
                 tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -225,6 +226,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            sdesc_sw128(ring_v(s) + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar(L::kBarSFull));
+                // then dQ for step j-1, once its dS is in TMEM
+                if (j > 0) {
+                    ok = fa_wait(bar(L::kBarDSFull), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
+                    if (!ok) break;
+                    issue_dq(j - 1);
+                }
             }
             if (ok && n_kv > 0) {
                 ok = fa_wait(bar(L::kBarDSFull), (uint32_t)((n_kv - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
@@ -252,8 +259,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             ok = fa_wait_warp(bar(L::kBarSFull), (uint32_t)(j & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            if (!ok) break;
+            tc_fence_after_sync();
+            // this warp's 64 columns of S and dP into registers, then release the
+            // columns to the next step's products
+            uint32_t sv[64], dv[64];
+            tmem_ld64_wait(t_lane + kColS + 64u * half, sv);
+            tmem_ld64_wait(t_lane + kColDP + 64u * half, dv);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarSRead));
             // dS(j-1) must have been read by its dQ product before it is overwritten
-            if (ok && j > 0)
+            if (j > 0)
                 ok = fa_wait_warp(bar(L::kBarUsed), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusSoftmaxWaitPV);
             if (!ok) break;
             tc_fence_after_sync();
@@ -263,16 +280,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
                 const int ch = 2 * half + hc;
-                uint32_t sv[32], dv[32], pk[16];
-                tmem_ld32_wait(t_lane + kColS + 32u * ch, sv);
-                tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
+                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int c0 = 32 * ch + 2 * i;
-                    const float p0 = (c0 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c2, -lse2)) : 0.f;
-                    const float p1 = (c0 + 1 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c2, -lse2)) : 0.f;
-                    pk[i] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * i]) - drow),
-                                        p1 * (__uint_as_float(dv[2 * i + 1]) - drow));
+                    const int c0 = 32 * ch + 2 * i, e = 32 * hc + 2 * i;
+                    const float p0 = (c0 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e]), c2, -lse2)) : 0.f;
+                    const float p1 = (c0 + 1 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), c2, -lse2)) : 0.f;
+                    pk[i] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - drow), p1 * (__uint_as_float(dv[e + 1]) - drow));
                 }
                 tmem_st16(t_lane + kColDS + 16u * ch, pk);
             }
