@@ -910,34 +910,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.ws_lbf[r] = l_fin;
                     p.ws_l32[r] = l32_fin;
                 }
+                // O has been read out of TMEM: the next tile's first P V may overwrite it
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kBarOFree));
             } else {
-                // O/l -> bf16, straight from registers to this thread's half row
+                // this thread's half row of O in one load; the next tile's first P V
+                // may overwrite O as soon as it is in registers
+                uint32_t r[kOCols];
+                if constexpr (kOCols == 64)
+                    tmem_ld64_wait(o_col, r);
+                else
+                    tmem_ld32_wait(o_col, r);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kBarOFree));
+                // O/l -> bf16, straight from registers to the half row: 32-byte
+                // stores when O is 32-byte aligned (full L2 sectors), else 16-byte.
+                // (Staging through shared memory for coalesced or tensor stores
+                // measured slower.)
                 const float inv_l = l_fin > 0.f ? 1.f / l_fin : 0.f;
-                uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                                       ((size_t)w.bh * (size_t)p.N + (size_t)q_idx) * D +
-                                                       wg * kOCols);
+                uint32_t wv[kOCols / 2];
 #pragma unroll
-                for (int c = 0; c < kOCols / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32_wait(o_col + 32u * c, r);
-                    uint32_t wv[16];
+                for (int i = 0; i < kOCols / 2; ++i)
+                    wv[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+                __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
+                                      ((size_t)w.bh * (size_t)p.N + (size_t)q_idx) * D + wg * kOCols;
+                if (valid) {
+                    if ((reinterpret_cast<uintptr_t>(p.o) & 31u) == 0) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        wv[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-                    if (valid) {
+                        for (int u = 0; u < kOCols / 16; ++u) st_global_v8(orow + 16 * u, wv + 8 * u);
+                    } else {
+                        uint4* o4 = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            orow[c * 4 + u] = make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
+                        for (int u = 0; u < kOCols / 8; ++u)
+                            o4[u] = make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
                     }
                 }
                 if (valid && wg == 0)
                     p.lse[(size_t)w.bh * (size_t)p.N + (size_t)q_idx] =
                         l32_fin > 0.f ? (m_fin + lg2_approx(l32_fin)) * kLn2 : -INFINITY;
             }
-            // O has been read out of TMEM: the next tile's first P V may overwrite it
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarOFree));
             ++t;
         }
         __syncwarp();

@@ -247,6 +247,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// 32-byte global store (address 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                 "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // two fp32 lanes in one 64-bit register (packed fp32x2 arithmetic)
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
     uint64_t r;

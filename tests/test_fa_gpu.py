@@ -182,6 +182,30 @@ def test_work_queue_across_calls_and_streams(fa):
         assert torch.equal(o, ro) and torch.equal(l, rl), which
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_alignment_and_bounds(fa, d):
+    """O at a 16-byte but not 32-byte aligned address, N ragged: the same values
+    as an aligned output, and nothing written outside O (rows past N are not
+    stored, by row stores or tensor stores)."""
+    B, H, N = 2, 3, 200
+    w = wl.Workload("al", B, H, N, d, True, "iid", 13)
+    q, k, v = (t.cuda() for t in wl.make_inputs(w))
+    ref_o, ref_l = fa.attention(q, k, v, causal=True)
+    n = B * H * N * d
+    pad = 64                                    # elements of sentinel on each side
+    buf = torch.full((n + 2 * pad + 8,), -7.0, dtype=torch.bfloat16, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    o = buf[pad + 8: pad + 8 + n]               # 16-byte aligned, 32-byte misaligned
+    assert o.data_ptr() % 16 == 0 and o.data_ptr() % 32 == 16
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    rc = fa.lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, 1,
+                         1.0 / math.sqrt(d), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert torch.equal(o.view(B, H, N, d), ref_o) and torch.equal(lse, ref_l)
+    assert torch.all(buf[:pad + 8] == -7.0) and torch.all(buf[pad + 8 + n:] == -7.0)
+
+
 def test_inputs_untouched(fa):
     w = wl.Workload("ro", 1, 2, 300, 64, False, "iid", 6)
     q, k, v = (t.cuda() for t in wl.make_inputs(w))
