@@ -147,6 +147,16 @@ def recorded_traffic(workload: str, kernel: str = KERNEL_NAME):
     return None
 
 
+def step_stats(ms_list):
+    """Min / median / max of the individually timed steps (rank 0's device time, ms)."""
+    if not ms_list:
+        return None
+    xs = sorted(ms_list)
+    n = len(xs)
+    med = xs[n // 2] if n % 2 else 0.5 * (xs[n // 2 - 1] + xs[n // 2])
+    return {"min": xs[0], "median": med, "max": xs[-1], "n": n}
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -649,7 +659,9 @@ def main():
     flush_l2 = in_bytes < 1.25 * L2_BYTES
     flusher = L2Flush(torch, dev) if flush_l2 else None
 
-    def timed(fn, n):
+    per_step = []  # this rank's device time of each timed step (ms)
+
+    def timed(fn, n, record_steps=False):
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
@@ -664,22 +676,26 @@ def main():
                 e1.record(stream)
                 e1.synchronize()
                 ms += e0.elapsed_time(e1)
+                if record_steps:
+                    per_step.append(e0.elapsed_time(e1))
         else:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(n):
+            # an event between consecutive steps gives each step's time as well
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            ev[0].record(stream)
+            for i in range(n):
                 fn()
-            e1.record(stream)
+                ev[i + 1].record(stream)
             torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1)
+            ms = ev[0].elapsed_time(ev[n])
+            if record_steps:
+                per_step.extend(ev[i].elapsed_time(ev[i + 1]) for i in range(n))
         ms = max_over_ranks(ms, dist, dev)
         if dist is not None:
             dist.barrier()
         return ms
 
     with ClockSampler(local_rank) as clk:
-        ms_total = timed(step, args.steps)
+        ms_total = timed(step, args.steps, record_steps=True)
     clocks = clk.summary()
     ms_step = ms_total / args.steps
     flops = workload_flops(w)
@@ -738,6 +754,7 @@ def main():
                     "ms_per_step": ms_e2e / args.steps},
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
+            "step_ms": step_stats(per_step),
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

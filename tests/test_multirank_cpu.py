@@ -69,3 +69,11 @@ def test_single_process_helpers():
     w = wl.WORKLOADS["B4-H16-N4096-d128-causal"]
     assert bench.workload_flops(w) == 4 * 4 * 16 * 4096 ** 2 * 128 / 2
     assert bench.rank_workload(w, 0).seed == w.seed
+
+
+def test_step_stats():
+    import bench
+
+    assert bench.step_stats([]) is None
+    assert bench.step_stats([3.0, 1.0, 2.0]) == {"min": 1.0, "median": 2.0, "max": 3.0, "n": 3}
+    assert bench.step_stats([4.0, 1.0, 2.0, 3.0])["median"] == 2.5
