@@ -137,7 +137,15 @@ struct FaSmem {
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffK = kOffQ + kQBufs * kTileBytes;
     static constexpr uint32_t kOffV = kOffK + NK * kTileBytes;
-    static constexpr uint32_t kOffBar = kOffV + NV * kTileBytes;
+    // d = 64 leaves TMEM room for the row sums of P on the tensor core: the P V
+    // product is widened to N = d + 16, and its B operand's second 64-column
+    // block (reached through the descriptor's leading-byte offset) is a 2 KB
+    // tile of ones, so columns d..d+15 of the accumulator receive the row sums
+    // of the same bf16 P (16 key rows x 128 bytes; any swizzle of ones is ones)
+    static constexpr bool kTcSum = D == 64;
+    static constexpr uint32_t kOnesBytes = kTcSum ? 2048u : 0u;
+    static constexpr uint32_t kOffOnes = kOffV + NV * kTileBytes;
+    static constexpr uint32_t kOffBar = kOffOnes + kOnesBytes;
     static constexpr int kBarQ = 0;  // per Q buffer: the tile landed
     static constexpr int kBarKFull = kBarQ + kQBufs;
     static constexpr int kBarKEmpty = kBarKFull + NK;
@@ -165,11 +173,13 @@ struct FaSmem {
     static constexpr uint32_t kBytes = kOffAbort + 4;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
     static_assert(kAlloc <= 232448u, "dynamic shared memory above the 227 KB a CTA may use");
-    // TMEM columns: S0 S1 O P0 P1
+    // TMEM columns: S0 S1 O [row sums] P0 P1
     __host__ __device__ static constexpr uint32_t col_s(int b) { return (uint32_t)b * 128u; }
     static constexpr uint32_t kColO = 256;
-    __host__ __device__ static constexpr uint32_t col_p(int b) { return 256u + D + (uint32_t)b * 64u; }
-    static_assert(256 + D + 128 <= (int)kTmemCols, "TMEM budget");
+    static constexpr uint32_t kSumCols = kTcSum ? 16u : 0u;
+    static constexpr uint32_t kColL = 256u + D;  // row sums of the bf16 P (kTcSum), column kColL
+    __host__ __device__ static constexpr uint32_t col_p(int b) { return 256u + D + kSumCols + (uint32_t)b * 64u; }
+    static_assert(256 + D + kSumCols + 128 <= kTmemCols, "TMEM budget");
 };
 
 // Bounded wait on an mbarrier phase.  Gives up when another warp of the CTA
@@ -216,7 +226,7 @@ __device__ __forceinline__ bool fa_wait_drain(uint32_t bar, uint32_t parity, uin
 
 // Exponentials of NE keys of a row against the reference -neg_m (base 2):
 // P packed to bf16 pairs, the sum of the bf16-rounded values and the fp32 sum.
-template <int NE>
+template <int NE, bool kBfSum = true>
 __device__ __forceinline__ void exp_row_tile(const float (&s)[NE], float c2, float neg_m, uint32_t (&pk)[NE / 2],
                                              float& sum_bf, float& sum_f32) {
     const uint64_t c2x2 = f32x2_pack(c2, c2), negm2 = f32x2_pack(neg_m, neg_m);
@@ -229,7 +239,7 @@ __device__ __forceinline__ void exp_row_tile(const float (&s)[NE], float c2, flo
         const float p0 = ex2_approx(x0);
         const float p1 = ex2_approx(x1);
         pk[i] = pack_bf16x2(p0, p1);
-        rs[i & 3] = add_bf16x2_f32(rs[i & 3], pk[i]);
+        if constexpr (kBfSum) rs[i & 3] = add_bf16x2_f32(rs[i & 3], pk[i]);
         r32[i & 1] = fadd2(r32[i & 1], f32x2_pack(p0, p1));
     }
     float e0, e1, o0, o1;
@@ -504,6 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
+    if constexpr (L::kTcSum) {
+        // the tile of ones (bf16 1.0 pairs) that the row-sum products read
+        uint32_t* ones = reinterpret_cast<uint32_t*>(smem + L::kOffOnes);
+        for (uint32_t i = threadIdx.x; i < L::kOnesBytes / 4u; i += blockDim.x) ones[i] = 0x3F803F80u;
+        fence_proxy_async_smem();
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -629,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // softmax warps have read the previous tile's O out of TMEM.
         // ------------------------------------------------------------------
         if (lane == 0) {
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D + L::kSumCols, false, true);
             int g = 0, t = 0;
             Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
             TileWork w;
@@ -649,10 +665,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t va = sbase + L::kOffV + (uint32_t)vs * L::kTileBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk)
-                        mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u,
-                               sdesc_sw128(va + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescPV,
-                               (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                        const uint32_t vk = va + (uint32_t)kk * 2048u;  // key rows 16 kk .. 16 kk + 15
+                        // second 64-column block: the next chunk of V (d = 128), or the
+                        // ones tile for the row sums (d = 64)
+                        const uint32_t lbo = L::kTcSum ? sbase + L::kOffOnes - vk : kChunkBytes;
+                        mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u, sdesc_sw128(vk, lbo, 1024),
+                               kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
                     tc_commit(bar(L::kBarVEmpty + vs));
                     tc_commit(bar(L::kBarPVDone + b));
                     if (j + 1 == w.n_kv) tc_commit(bar(L::kBarOFinal));
@@ -822,7 +842,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // -inf scores give 0 rather than NaN
                 uint32_t pk[kBlockN / 2];
                 float sum_bf, sum_f32;
-                exp_row_tile<kBlockN>(s, c2, (m_new == -INFINITY) ? 0.f : -m_new, pk, sum_bf, sum_f32);
+                // with the sums on the tensor core (d = 64) only the fp32 sum is kept here
+                exp_row_tile<kBlockN, !L::kTcSum>(s, c2, (m_new == -INFINITY) ? 0.f : -m_new, pk, sum_bf, sum_f32);
                 l_run = l_run * a_l + sum_bf;
                 l32_run = l32_run * a_l + sum_f32;
                 if (g >= 2) {
@@ -857,6 +878,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st128(t_lane + L::kColO, r);
                     else
                         tmem_st64(t_lane + L::kColO, r);
+                    if constexpr (L::kTcSum) {
+                        // the row sums move to the new reference with O
+                        const uint32_t lv = tmem_ld1_wait(t_lane + L::kColL);
+                        tmem_st1(t_lane + L::kColL, __float_as_uint(__uint_as_float(lv) * a_o));
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before_sync();
@@ -887,6 +913,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = fa_wait_warp(bar(L::kBarOFinal), (uint32_t)(t & 1), abort_flag, limit, kStatusSoftmaxWaitO);
             if (!ok) break;
             tc_fence_after_sync();
+            // the tensor-core row sums are in the reference of the tile's last step,
+            // the largest one, m_fin (references only grow), like O
+            if constexpr (L::kTcSum) l_fin = __uint_as_float(tmem_ld1_wait(t_lane + L::kColL));
             const uint32_t o_col = t_lane + L::kColO + (uint32_t)(wg * kOCols);
             if constexpr (kSplit) {
                 // partial state of this split: unnormalised O and (m, sums) per row.
