@@ -193,6 +193,43 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 int fa_splitkv_auto_splits(int B, int H, int N, int d, int causal);
 
 /*
+ * fa_fwd_host -- fa_fwd on HOST-resident tensors, streamed through the GPU.
+ *
+ * Arguments as for fa_fwd, except that q, k, v, o and lse are host pointers.
+ * They must be pinned (page-locked, e.g. cudaHostAlloc) for the copies to
+ * overlap the compute; pageable memory works but serialises.  Layouts are
+ * unchanged ([B][H][N][d] bf16, lse [B][H][N] fp32), because the heads are
+ * independent problems ("Online Softmax: Tiling Across a Reduction": each
+ * query row's softmax needs only its own scores).  The call walks the B*H
+ * heads in chunks of heads_per_chunk through two device slots in `workspace`,
+ * on three streams.  It copies chunk c+1 to the device, runs the forward kernel
+ * on chunk c, and copies chunk c-1's o and lse back, all at once.
+ *
+ *   heads_per_chunk  1 .. B*H, or 0 for ceil(B*H / 8)
+ *   workspace        device memory, 256-byte aligned, at least
+ *                    fa_fwd_host_workspace_bytes(B, H, N, d, heads_per_chunk)
+ *                    bytes; owned by the caller, reusable once the call's work
+ *                    on `stream` has completed
+ *   stream           the caller's stream: the kernels run on it, and every copy
+ *                    is ordered after the work already on it and before the work
+ *                    enqueued on it afterwards (the call returns after enqueueing
+ *                    and does not synchronise)
+ *
+ * Two internal copy streams per device are created on first use and kept.  The
+ * enqueue of concurrent calls on one device is serialised by a lock.  Results
+ * are identical to fa_fwd's, bit for bit.  Returns FA_OK, an fa_fwd argument
+ * error, FA_ERR_SHAPE for heads_per_chunk outside 0..B*H, FA_ERR_NULL_POINTER or
+ * FA_ERR_ALIGNMENT for the workspace, FA_ERR_WORKSPACE, FA_ERR_DEVICE,
+ * FA_ERR_TENSOR_MAP or FA_ERR_CUDA.
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                int causal, float scale, int heads_per_chunk, void* workspace, size_t workspace_bytes,
+                fa_stream_t stream);
+
+/* Device workspace fa_fwd_host needs (two slots of one chunk's q, k, v, o and lse); 0 for bad arguments. */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chunk);
+
+/*
  * fa_bwd -- attention backward pass: the gradients of L = sum(O * dO) with
  * respect to q, k and v, for the forward of fa_fwd.  Nothing of the N x N
  * weights is read back: the scores are recomputed tile by tile from q and k

@@ -67,6 +67,10 @@ def lib() -> ctypes.CDLL:
             L.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
             L.fa_splitkv_auto_splits.argtypes = [I, I, I, I, I]
             L.fa_splitkv_auto_splits.restype = I
+            L.fa_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, ctypes.c_size_t, P]
+            L.fa_fwd_host.restype = I
+            L.fa_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I]
+            L.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
             L.fa_strerror.argtypes = [I]
             L.fa_strerror.restype = ctypes.c_char_p
             L.fa_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
@@ -111,6 +115,19 @@ def _stream(stream) -> int:
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def _host_ptr(x) -> int:
+    """Address of a contiguous CPU tensor (the host side of fa_fwd_host)."""
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if x.is_cuda:
+            raise ValueError("fa_fwd_host takes host (CPU) tensors")
+        if not x.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        return x.data_ptr()
+    raise TypeError(f"cannot take a host pointer from {type(x)!r}")
 
 
 def fa_strerror(code: int) -> str:
@@ -199,6 +216,45 @@ def fa_splitkv_workspace_bytes(B: int, H: int, N: int, d: int, n_splits: int) ->
 
 def fa_splitkv_auto_splits(B: int, H: int, N: int, d: int, causal: bool) -> int:
     return int(lib().fa_splitkv_auto_splits(int(B), int(H), int(N), int(d), 1 if causal else 0))
+
+
+def fa_fwd_host(q, k, v, o, lse, B: int, H: int, N: int, d: int, causal: bool, scale: float, heads_per_chunk: int,
+                workspace, workspace_bytes: int, stream=None) -> None:
+    """Enqueue the forward on host tensors (q, k, v, o, lse on the CPU, pinned for
+    overlap), streamed through a device workspace; raises FaError on a nonzero C return code."""
+    rc = lib().fa_fwd_host(_host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(o), _host_ptr(lse), int(B), int(H),
+                           int(N), int(d), 1 if causal else 0, float(scale), int(heads_per_chunk), _ptr(workspace),
+                           int(workspace_bytes), _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+
+
+def fa_fwd_host_workspace_bytes(B: int, H: int, N: int, d: int, heads_per_chunk: int = 0) -> int:
+    return int(lib().fa_fwd_host_workspace_bytes(int(B), int(H), int(N), int(d), int(heads_per_chunk)))
+
+
+def attention_host(q, k, v, causal: bool = False, scale: float | None = None, heads_per_chunk: int = 0,
+                   workspace=None, out=None, stream=None):
+    """Forward on CPU bf16 tensors [B, H, N, d]: returns CPU (o, lse), pinned.
+    The call is asynchronous on `stream`; synchronise before reading the outputs.
+    Allocates the device workspace with torch when none is given."""
+    import torch
+
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("q, k and v must be bfloat16")
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    need = fa_fwd_host_workspace_bytes(B, H, N, d, heads_per_chunk)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if out is None:
+        out = (torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True),
+               torch.empty((B, H, N), dtype=torch.float32, pin_memory=True))
+    o, lse = out
+    fa_fwd_host(q, k, v, o, lse, B, H, N, d, causal, (1.0 / math.sqrt(d)) if scale is None else scale,
+                heads_per_chunk, workspace, workspace.numel() * workspace.element_size(), stream)
+    return o, lse
 
 
 def attention_splitkv(q, k, v, causal: bool = False, scale: float | None = None, n_splits: int = 0, workspace=None,

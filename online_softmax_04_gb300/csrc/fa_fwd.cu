@@ -76,6 +76,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 int sm_count();
+int queue_slot(unsigned int** out);
 
 // kSplit: one CTA per (query tile, head, key split).  Otherwise a persistent
 // grid of at most one CTA per SM walks the work items (see fa::TileSeq).
@@ -92,6 +93,9 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
         // blockIdx.x runs from the last (longest causal) tile down: heaviest first
         grid = dim3((unsigned)p.n_tiles, (unsigned)BH, (unsigned)p.n_splits);
     } else {
+        // every persistent launch takes its own work counter (the dynamic tail)
+        const int qrc = queue_slot(&p.queue);
+        if (qrc != FA_OK) return qrc;
         const int sms = sm_count() > 0 ? sm_count() : 148;
         const long long pairs = fa::persistent_pairs(p);
         const long long tiles = (long long)BH * p.n_tiles;
@@ -265,6 +269,57 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// fa_fwd_host: host-resident tensors streamed through two device slots
+// ---------------------------------------------------------------------------
+constexpr size_t kHostAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int host_chunk_heads(long long BH, int heads_per_chunk) {
+    return heads_per_chunk > 0 ? heads_per_chunk : (int)((BH + 7) / 8);
+}
+
+// one slot: q, k, v, o (bf16) and lse (fp32) of `hc` heads, each 256-byte aligned
+size_t host_slot_bytes(int hc, int N, int d) {
+    const size_t t = align_up((size_t)hc * (size_t)N * (size_t)d * 2u, kHostAlign);
+    return 4 * t + align_up((size_t)hc * (size_t)N * 4u, kHostAlign);
+}
+
+// The two copy streams and the events of the pipeline, per device, made on
+// first use and kept for the life of the process.  (Separate input streams
+// for q, k and v measured slower: the host link, not the copy engines, limits.)
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t in_done[2] = {}, compute_done[2] = {}, out_done[2] = {};
+};
+HostPipe g_host_pipe[kMaxDevices];
+std::mutex g_host_mu;  // serialises the enqueue of fa_fwd_host calls (shared streams and events)
+
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+    HostPipe& hp = g_host_pipe[dev];
+    if (!hp.ready) {
+        const unsigned ev = cudaEventDisableTiming;
+        bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp.start, ev) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp.end, ev) == cudaSuccess;
+        for (int i = 0; ok && i < 2; ++i)
+            ok = cudaEventCreateWithFlags(&hp.in_done[i], ev) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&hp.compute_done[i], ev) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&hp.out_done[i], ev) == cudaSuccess;
+        if (!ok) return FA_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -275,8 +330,6 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (rc != FA_OK) return rc;
     Prepared pr;
     rc = prepare(q, k, v, o, lse, B, H, N, d, causal, scale, &pr);
-    if (rc != FA_OK) return rc;
-    rc = queue_slot(&pr.p.queue);
     if (rc != FA_OK) return rc;
     return launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -299,8 +352,6 @@ int fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* l
     pr.p.window_left = window_left;
     pr.p.window_right = window_right;
     pr.p.doc = doc_ids;
-    rc = queue_slot(&pr.p.queue);
-    if (rc != FA_OK) return rc;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // full or causal attention without documents takes the unmasked kernel
     if (window_left < 0 && (window_right < 0 || window_right == 0) && !doc_ids)
@@ -422,6 +473,77 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
         fa::fa_splitkv_merge<128><<<blocks, 256, 0, s>>>(pr.p.ws_o, pr.p.ws_m, pr.p.ws_lbf, pr.p.ws_l32, ob, lse,
                                                          rows, n_splits);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chunk) {
+    if ((d != 64 && d != 128) || B < 1 || H < 1 || N < 1) return 0;
+    const long long BH = (long long)B * (long long)H;
+    if (heads_per_chunk < 0 || heads_per_chunk > BH) return 0;
+    return 2 * host_slot_bytes(host_chunk_heads(BH, heads_per_chunk), N, d);
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                int causal, float scale, int heads_per_chunk, void* workspace, size_t workspace_bytes,
+                fa_stream_t stream) {
+    int rc = validate(q, k, v, o, lse, B, H, N, d, scale);
+    if (rc != FA_OK) return rc;
+    const long long BH = (long long)B * (long long)H;
+    if (heads_per_chunk < 0 || heads_per_chunk > BH) return FA_ERR_SHAPE;
+    if (!workspace) return FA_ERR_NULL_POINTER;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kHostAlign - 1)) != 0) return FA_ERR_ALIGNMENT;
+    const int hc = host_chunk_heads(BH, heads_per_chunk);
+    const size_t slot = host_slot_bytes(hc, N, d);
+    if (workspace_bytes < 2 * slot) return FA_ERR_WORKSPACE;
+    rc = check_device();
+    if (rc != FA_OK) return rc;
+
+    std::lock_guard<std::mutex> lk(g_host_mu);
+    HostPipe* hp = nullptr;
+    rc = host_pipe(&hp);
+    if (rc != FA_OK) return rc;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t head_elems = (size_t)N * (size_t)d;
+    const size_t tbytes = align_up((size_t)hc * head_elems * 2u, kHostAlign);
+    bool ok = cudaEventRecord(hp->start, cs) == cudaSuccess && cudaStreamWaitEvent(hp->h2d, hp->start, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(hp->d2h, hp->start, 0) == cudaSuccess;
+    const long long n_chunks = (BH + hc - 1) / hc;
+    for (long long c = 0; ok && c < n_chunks; ++c) {
+        const int sl = (int)(c & 1);
+        const long long h0 = c * hc;
+        const int nh = (int)std::min<long long>(hc, BH - h0);
+        uint8_t* base = static_cast<uint8_t*>(workspace) + (size_t)sl * slot;
+        void* dq = base;
+        void* dk = base + tbytes;
+        void* dv = base + 2 * tbytes;
+        void* dout = base + 3 * tbytes;
+        float* dlse = reinterpret_cast<float*>(base + 4 * tbytes);
+        const size_t off = (size_t)h0 * head_elems * 2u;  // byte offset of the chunk's first head
+        const size_t bytes = (size_t)nh * head_elems * 2u;
+        // inputs: once the slot's previous chunk has been read back
+        if (c >= 2) ok = cudaStreamWaitEvent(hp->h2d, hp->out_done[sl], 0) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + off, bytes, cudaMemcpyDefault, hp->h2d) == cudaSuccess &&
+             cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + off, bytes, cudaMemcpyDefault, hp->h2d) == cudaSuccess &&
+             cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + off, bytes, cudaMemcpyDefault, hp->h2d) == cudaSuccess &&
+             cudaEventRecord(hp->in_done[sl], hp->h2d) == cudaSuccess &&
+             cudaStreamWaitEvent(cs, hp->in_done[sl], 0) == cudaSuccess;
+        if (!ok) break;
+        // the kernel, on the caller's stream: the chunk's heads as one batch
+        Prepared pr;
+        rc = prepare(dq, dk, dv, dout, dlse, 1, nh, N, d, causal, scale, &pr);
+        if (rc != FA_OK) return rc;
+        rc = launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, cs);
+        if (rc != FA_OK) return rc;
+        // outputs
+        ok = cudaEventRecord(hp->compute_done[sl], cs) == cudaSuccess &&
+             cudaStreamWaitEvent(hp->d2h, hp->compute_done[sl], 0) == cudaSuccess &&
+             cudaMemcpyAsync(static_cast<uint8_t*>(o) + off, dout, bytes, cudaMemcpyDefault, hp->d2h) == cudaSuccess &&
+             cudaMemcpyAsync(lse + (size_t)h0 * (size_t)N, dlse, (size_t)nh * (size_t)N * 4u, cudaMemcpyDefault,
+                             hp->d2h) == cudaSuccess &&
+             cudaEventRecord(hp->out_done[sl], hp->d2h) == cudaSuccess;
+    }
+    // the caller's stream continues after the last read-back
+    ok = ok && cudaEventRecord(hp->end, hp->d2h) == cudaSuccess && cudaStreamWaitEvent(cs, hp->end, 0) == cudaSuccess;
+    return ok ? FA_OK : FA_ERR_CUDA;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -179,3 +179,31 @@ def test_splitkv_workspace_formula(fa):
     # automatic count: never more than the key tiles, 1 once the plain grid fills the GPU
     assert 1 <= fa.fa_splitkv_auto_splits(1, 1, 256, 64, 0) <= 2
     assert fa.fa_splitkv_auto_splits(1, 32, 16384, 128, 1) == 1
+
+
+def test_host_streamed_validation(fa):
+    """fa_fwd_host: argument checks that need no GPU, and the workspace size rule."""
+    L = fa.lib()
+    q, k, v, o, lse = FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30), FAKE + (4 << 30)
+    ws = FAKE + (5 << 30)
+    B, H, N, d = 2, 3, 200, 64
+    need = fa.fa_fwd_host_workspace_bytes(B, H, N, d, 2)
+    # two slots of 2 heads: q, k, v, o (2*200*64*2 = 51200 B each, 256-aligned) and lse (1600 -> 1792 B)
+    assert need == 2 * (4 * 51200 + 1792)
+    assert fa.fa_fwd_host_workspace_bytes(B, H, N, d, 0) == 2 * (4 * 25600 + 1024)  # ceil(6 / 8) = 1 head
+    assert fa.fa_fwd_host_workspace_bytes(B, H, N, d, 7) == 0
+    assert fa.fa_fwd_host_workspace_bytes(B, H, N, 96, 1) == 0
+
+    def call(hpc=2, w=ws, wb=need, **kw):
+        a = dict(q=q, k=k, v=v, o=o, lse=lse, d=d)
+        a.update(kw)
+        return L.fa_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], B, H, N, a["d"], 1, 0.125, hpc, w, wb, 0)
+
+    assert call(q=0) == fa.FA_ERR_NULL_POINTER
+    assert call(d=96) == fa.FA_ERR_HEAD_DIM
+    assert call(hpc=-1) == fa.FA_ERR_SHAPE
+    assert call(hpc=B * H + 1) == fa.FA_ERR_SHAPE
+    assert call(w=0) == fa.FA_ERR_NULL_POINTER
+    assert call(w=ws + 128) == fa.FA_ERR_ALIGNMENT
+    assert call(wb=need - 1) == fa.FA_ERR_WORKSPACE
+    assert call(o=q + 64) == fa.FA_ERR_ALIAS
