@@ -277,18 +277,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // keys visible to this row in this tile: c <= last
             int last = p.N - 1 - j * 128;
             if (p.causal && j == qt) last = min(last, row);
+            if (__all_sync(0xffffffffu, last >= 127)) {
+                // every key of the tile visible to every row of the warp: packed
+                // fp32x2 arithmetic, no masks
+                const uint64_t c2x2 = f32x2_pack(c2, c2), nl2 = f32x2_pack(-lse2, -lse2),
+                               nd2 = f32x2_pack(-drow, -drow);
 #pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                const int ch = 2 * half + hc;
-                uint32_t pk[16];
+                for (int hc = 0; hc < 2; ++hc) {
+                    const int ch = 2 * half + hc;
+                    uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c0 = 32 * ch + 2 * i, e = 32 * hc + 2 * i;
-                    const float p0 = (c0 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e]), c2, -lse2)) : 0.f;
-                    const float p1 = (c0 + 1 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), c2, -lse2)) : 0.f;
-                    pk[i] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - drow), p1 * (__uint_as_float(dv[e + 1]) - drow));
+                    for (int i = 0; i < 16; ++i) {
+                        const int e = 32 * hc + 2 * i;
+                        float x0, x1;
+                        f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, nl2),
+                                     x0, x1);
+                        const uint64_t pp = f32x2_pack(ex2_approx(x0), ex2_approx(x1));
+                        float d0, d1;
+                        f32x2_unpack(
+                            fmul2(pp, fadd2(f32x2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)), d0,
+                            d1);
+                        pk[i] = pack_bf16x2(d0, d1);
+                    }
+                    tmem_st16(t_lane + kColDS + 16u * ch, pk);
                 }
-                tmem_st16(t_lane + kColDS + 16u * ch, pk);
+            } else {
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {
+                    const int ch = 2 * half + hc;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int c0 = 32 * ch + 2 * i, e = 32 * hc + 2 * i;
+                        const float p0 = (c0 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e]), c2, -lse2)) : 0.f;
+                        const float p1 =
+                            (c0 + 1 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), c2, -lse2)) : 0.f;
+                        pk[i] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - drow),
+                                            p1 * (__uint_as_float(dv[e + 1]) - drow));
+                    }
+                    tmem_st16(t_lane + kColDS + 16u * ch, pk);
+                }
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -469,38 +497,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int i = 0; i < n_q; ++i) {
             const int qi = i0 + i;
-            // this query tile's LSE (log2 units) and D, staged once per warp; queries
-            // past N get LSE = +inf, so their weights are 0
+            // this query tile's -LSE (log2 units) and -D, staged once per warp; queries
+            // past N get -LSE = -inf, so their weights are 0
             float* st = stage + (i & 1) * 256;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int c = u * 32 + lane;
                 const int q = qi * 128 + c;
                 const size_t r = (size_t)bh * p.N + (size_t)q;
-                st[c] = q < p.N ? p.lse[r] * kLog2e : INFINITY;
-                st[128 + c] = q < p.N ? p.delta[r] : 0.f;
+                st[c] = q < p.N ? -(p.lse[r] * kLog2e) : -INFINITY;
+                st[128 + c] = q < p.N ? -p.delta[r] : 0.f;
             }
             __syncwarp();
             ok = fa_wait_warp(bar(L::kBarSFull), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
             if (!ok) break;
             tc_fence_after_sync();
             // causal: query q sees key k_idx iff k_idx <= q, i.e. column c >= first
-            const int first = (p.causal && qi == kt) ? row : 0;
+            // (only the diagonal tile masks; queries past N weigh 0 through -LSE)
+            const bool diag = p.causal && qi == kt;
+            const int first = diag ? row : 0;
+            const uint64_t c2x2 = f32x2_pack(c2, c2);
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
                 const int ch = 2 * half + hc;
                 uint32_t sv[32], dv[32], pk[16], dk[16];
                 tmem_ld32_wait(t_lane + kColS + 32u * ch, sv);
                 tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
+                if (!diag) {
+                    // packed fp32x2 arithmetic; -LSE and -D of two queries per load
 #pragma unroll
-                for (int i2 = 0; i2 < 16; ++i2) {
-                    const int c0 = 32 * ch + 2 * i2;
-                    const float p0 = (c0 >= first) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i2]), c2, -st[c0])) : 0.f;
-                    const float p1 =
-                        (c0 + 1 >= first) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i2 + 1]), c2, -st[c0 + 1])) : 0.f;
-                    pk[i2] = pack_bf16x2(p0, p1);
-                    dk[i2] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * i2]) - st[128 + c0]),
-                                         p1 * (__uint_as_float(dv[2 * i2 + 1]) - st[128 + c0 + 1]));
+                    for (int i2 = 0; i2 < 16; ++i2) {
+                        const int c0 = 32 * ch + 2 * i2;
+                        const float2 nl = *reinterpret_cast<const float2*>(st + c0);
+                        const float2 nd = *reinterpret_cast<const float2*>(st + 128 + c0);
+                        float x0, x1;
+                        f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(sv[2 * i2]), __uint_as_float(sv[2 * i2 + 1])),
+                                           c2x2, f32x2_pack(nl.x, nl.y)),
+                                     x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        pk[i2] = pack_bf16x2(p0, p1);
+                        float d0, d1;
+                        f32x2_unpack(fmul2(f32x2_pack(p0, p1),
+                                           fadd2(f32x2_pack(__uint_as_float(dv[2 * i2]), __uint_as_float(dv[2 * i2 + 1])),
+                                                 f32x2_pack(nd.x, nd.y))),
+                                     d0, d1);
+                        dk[i2] = pack_bf16x2(d0, d1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i2 = 0; i2 < 16; ++i2) {
+                        const int c0 = 32 * ch + 2 * i2;
+                        const float p0 =
+                            (c0 >= first) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i2]), c2, st[c0])) : 0.f;
+                        const float p1 =
+                            (c0 + 1 >= first) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i2 + 1]), c2, st[c0 + 1])) : 0.f;
+                        pk[i2] = pack_bf16x2(p0, p1);
+                        dk[i2] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * i2]) + st[128 + c0]),
+                                             p1 * (__uint_as_float(dv[2 * i2 + 1]) + st[128 + c0 + 1]));
+                    }
                 }
                 // P^T and dS^T of query columns [64 half, +64) go to columns
                 // [64 half, 64 half + 32): inside what this warp has already read
