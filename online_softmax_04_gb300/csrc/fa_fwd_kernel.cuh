@@ -51,7 +51,12 @@
 //     depend on m, so the result is unchanged.
 //   * O is divided by the sum of the bf16-rounded exponentials, the very
 //     weights the P V product uses, so O / l is a convex combination of V
-//     rows; LSE uses the fp32 sum of the unrounded exponentials.
+//     rows; LSE uses the fp32 sum of the unrounded exponentials.  At d = 128
+//     the softmax threads add the rounded weights; at d = 64 the tensor core
+//     does, in extra columns of the P V product (see FaSmem::kTcSum).
+//   * Epilogue: each group reads its half of O's columns out of TMEM in one
+//     load, releases O to the next tile's first P V product at once, then
+//     normalises and stores its half rows.
 //   * Causal: key tiles wholly after the query tile are never visited; only
 //     the diagonal tile is masked element by element ("Online Softmax: Tiling
 //     Across a Reduction", causal section).  Keys >= N in the last tile are
