@@ -123,13 +123,39 @@ def measured_peak(key: str = "bf16_tflops"):
         return (FALLBACK_BF16_TFLOPS if key == "bf16_tflops" else FALLBACK_HBM_GBS), "fallback"
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source without its comments (string literals kept), for hashing what compiles."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash() -> str:
+    """sha256 prefix of online_softmax_04_gb300/csrc/*, comments removed: a traffic record
+    stays valid across comment edits and lapses with any change to what compiles."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "online_softmax_04_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(strip_c_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -77,3 +77,14 @@ def test_step_stats():
     assert bench.step_stats([]) is None
     assert bench.step_stats([3.0, 1.0, 2.0]) == {"min": 1.0, "median": 2.0, "max": 3.0, "n": 3}
     assert bench.step_stats([4.0, 1.0, 2.0, 3.0])["median"] == 2.5
+
+
+def test_source_hash_ignores_comments():
+    import bench
+
+    code = 'int a = 1;\nconst char* s = "// kept /* kept */";\nchar q = \'"\';\n'
+    with_comments = 'int a = 1; // one\n/* block\n comment */const char* s = "// kept /* kept */";\nchar q = \'"\'; // q\n'
+    strip = bench.strip_c_comments
+    assert strip(code) == code
+    assert strip(with_comments).split() == strip(code).split()
+    assert strip("int x; /* unterminated") == "int x;  "
