@@ -91,8 +91,8 @@ struct BwdSmem {
     static constexpr int kBarDSFull = kBarSFull + 1;    // compute warps wrote the bf16 operand(s)
     static constexpr int kBarUsed = kBarDSFull + 1;     // the products reading those operands finished
     static constexpr int kBarFinal = kBarUsed + 1;      // the accumulators are complete
-    static constexpr int kBarDrain = kBarFinal + 1;
-    static constexpr int kBarSRead = kBarDrain + 1;     // dQ kernel: the compute warps hold S and dP in registers
+    static constexpr int kBarDrain = kBarFinal + 1;     // [2] per MMA issuer
+    static constexpr int kBarSRead = kBarDrain + 2;     // dQ kernel: the compute warps hold S and dP in registers
     static constexpr int kNumBars = kBarSRead + 1;
     static constexpr uint32_t kOffStage = kOffBar + kNumBars * 8;     // [8 warps][2][LSE 128, D 128] floats
     static constexpr uint32_t kOffTmemSlot = kOffStage + 8 * 2 * 256 * 4;
@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::kBarUsed), 1);
         mbar_init(bar(L::kBarFinal), 1);
         mbar_init(bar(L::kBarDrain), 1);
+        mbar_init(bar(L::kBarDrain + 1), 1);
         mbar_init(bar(L::kBarSRead), 8);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -189,26 +190,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
+        // score products: S_j = Q K_j^T and dP_j = dO V_j^T, as soon as K_j, V_j
+        // have landed and the compute warps hold S_{j-1}, dP_{j-1} in registers
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, false, true);
             bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
-            auto issue_dq = [&](int jj) {  // dQ += dS K_jj once dS(jj) is in TMEM
-                const int s = jj % NS;
-                tc_fence_after_sync();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + kColDS + (uint32_t)kk * 8u,
-                           sdesc_sw128(ring_k(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescDQ,
-                           (jj > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar(L::kBarEmpty + s));
-                tc_commit(bar(L::kBarUsed));
-            };
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int s = j % NS;
                 ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
-                // S and dP of step j-1 are in the compute warps' registers: the next
-                // score products may overwrite their columns while dS(j-1) is formed
                 if (ok && j > 0)
                     ok = fa_wait(bar(L::kBarSRead), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusMmaWaitSFree);
                 if (!ok) break;
@@ -226,22 +215,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            sdesc_sw128(ring_v(s) + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar(L::kBarSFull));
-                // then dQ for step j-1, once its dS is in TMEM
-                if (j > 0) {
-                    ok = fa_wait(bar(L::kBarDSFull), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
-                    if (!ok) break;
-                    issue_dq(j - 1);
-                }
-            }
-            if (ok && n_kv > 0) {
-                ok = fa_wait(bar(L::kBarDSFull), (uint32_t)((n_kv - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
-                if (ok) {
-                    issue_dq(n_kv - 1);
-                    tc_commit(bar(L::kBarFinal));
-                }
             }
             tc_commit(bar(L::kBarDrain));
             fa_wait_drain(bar(L::kBarDrain), 0, limit);
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // gradient products, on a second issuing thread so that they overlap the
+        // next step's score products: dQ += dS_j K_j once dS_j is in TMEM
+        if (lane == 0) {
+            constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, false, true);
+            bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int s = j % NS;
+                ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK) &&
+                     fa_wait(bar(L::kBarDSFull), (uint32_t)(j & 1), abort_flag, limit, kStatusMmaWaitP);
+                if (!ok) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColDQ, tmem + kColDS + (uint32_t)kk * 8u,
+                           sdesc_sw128(ring_k(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescDQ,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                // S_j and dP_j finished before dS_j was written, so this covers every
+                // product that read stage s
+                tc_commit(bar(L::kBarEmpty + s));
+                tc_commit(bar(L::kBarUsed));
+            }
+            if (ok && n_kv > 0) tc_commit(bar(L::kBarFinal));
+            tc_commit(bar(L::kBarDrain + 1));
+            fa_wait_drain(bar(L::kBarDrain + 1), 0, limit);
         }
         __syncwarp();
     } else if (warp >= 4) {
