@@ -89,8 +89,8 @@ struct BwdSmem {
     static constexpr int kBarEmpty = kBarFull + NS;     // [NS] stage consumed by the MMAs
     static constexpr int kBarSFull = kBarEmpty + NS;    // the two score-like products of a step finished
     static constexpr int kBarDSFull = kBarSFull + 1;    // compute warps wrote the bf16 operand(s)
-    static constexpr int kBarUsed = kBarDSFull + 1;     // the products reading those operands finished
-    static constexpr int kBarFinal = kBarUsed + 1;      // the accumulators are complete
+    static constexpr int kBarUsed = kBarDSFull + 1;     // [2] the products reading those operands finished
+    static constexpr int kBarFinal = kBarUsed + 2;      // the accumulators are complete
     static constexpr int kBarDrain = kBarFinal + 1;     // [2] per MMA issuer
     static constexpr int kBarSRead = kBarDrain + 2;     // dQ kernel: the compute warps hold S and dP in registers
     static constexpr int kNumBars = kBarSRead + 1;
@@ -386,13 +386,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::kBarRes), 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar(L::kBarFull + s), 1);
-            mbar_init(bar(L::kBarEmpty + s), 1);
+            mbar_init(bar(L::kBarEmpty + s), 2);  // both issuers' products read the stage
         }
-        mbar_init(bar(L::kBarSFull), 1);
+        mbar_init(bar(L::kBarSFull), 2);  // both issuers
         mbar_init(bar(L::kBarDSFull), 8);
-        mbar_init(bar(L::kBarUsed), 1);
-        mbar_init(bar(L::kBarFinal), 1);
+        mbar_init(bar(L::kBarUsed + 0), 1);  // dV products (warp 1)
+        mbar_init(bar(L::kBarUsed + 1), 1);  // dK products (warp 3)
+        mbar_init(bar(L::kBarFinal), 2);
         mbar_init(bar(L::kBarDrain), 1);
+        mbar_init(bar(L::kBarDrain + 1), 1);
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_q);
@@ -436,31 +438,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 3) {
+        // Two issuing threads, so that two MMA streams run at once: warp 1 issues
+        // S^T = K Q_i^T and then dV += P^T dO_i, warp 3 issues dP^T = V dO_i^T and
+        // then dK += dS^T Q_i.  Each thread's score product overwrites the columns
+        // its own gradient product of step i-1 read, so it waits for that product.
         if (lane == 0) {
+            const int u = warp == 1 ? 0 : 1;  // 0: S / dV, 1: dP / dK
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);
+            const uint32_t res_a = u == 0 ? res_k : res_v;  // K for S^T, V for dP^T
+            const uint32_t col_sc = u == 0 ? kColS : kColDP;
+            const uint32_t col_acc = u == 0 ? kColDV : kColDK;
             bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
             for (int i = 0; ok && i < n_q; ++i) {
                 const int s = i % NS;
+                const uint32_t b_sc = u == 0 ? ring_q(s) : ring_do(s);   // B of the score product
+                const uint32_t b_acc = u == 0 ? ring_do(s) : ring_q(s);  // B of the gradient product
                 ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((i / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
-                // the columns of S^T and dP^T hold P^T and dS^T of step i-1 until its
-                // dV and dK products have finished
+                // this thread's score columns hold its bf16 operand of step i-1 until its
+                // gradient product has finished
                 if (ok && i > 0)
-                    ok = fa_wait(bar(L::kBarUsed), (uint32_t)((i - 1) & 1), abort_flag, limit, kStatusMmaWaitSFree);
+                    ok = fa_wait(bar(L::kBarUsed + u), (uint32_t)((i - 1) & 1), abort_flag, limit, kStatusMmaWaitSFree);
                 if (!ok) break;
                 tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + kColS, sdesc_sw128(res_k + off, 16, 1024), sdesc_sw128(ring_q(s) + off, 16, 1024),
-                           kIdescS, kk > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + kColDP, sdesc_sw128(res_v + off, 16, 1024),
-                           sdesc_sw128(ring_do(s) + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + col_sc, sdesc_sw128(res_a + off, 16, 1024), sdesc_sw128(b_sc + off, 16, 1024), kIdescS,
+                           kk > 0 ? 1u : 0u);
                 }
                 tc_commit(bar(L::kBarSFull));
                 ok = fa_wait(bar(L::kBarDSFull), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
@@ -470,22 +476,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // 8 kk (first half of the queries) or 32 + 8 kk (second half)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    mma_ts(tmem + kColDV, tmem + kColS + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
-                           sdesc_sw128(ring_do(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescG,
-                           (i > 0 || kk > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    mma_ts(tmem + kColDK, tmem + kColDP + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
-                           sdesc_sw128(ring_q(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescG,
+                    mma_ts(tmem + col_acc, tmem + col_sc + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
+                           sdesc_sw128(b_acc + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescG,
                            (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(L::kBarEmpty + s));
-                tc_commit(bar(L::kBarUsed));
+                tc_commit(bar(L::kBarUsed + u));
             }
             if (ok && n_q > 0) tc_commit(bar(L::kBarFinal));
-            tc_commit(bar(L::kBarDrain));
-            fa_wait_drain(bar(L::kBarDrain), 0, limit);
+            tc_commit(bar(L::kBarDrain + u));
+            fa_wait_drain(bar(L::kBarDrain + u), 0, limit);
         }
         __syncwarp();
     } else if (warp >= 4) {
