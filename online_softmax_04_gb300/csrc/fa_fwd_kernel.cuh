@@ -730,13 +730,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
             }
-            // this row's visible keys, [row_lo, row_hi] (sequence positions), before documents;
-            // rows past N see every key (they are never stored)
-            int row_lo = 0, row_hi = p.N - 1, my_doc = 0;
+            // this row's visible keys, [row_lo, row_hi] (sequence positions): the window
+            // intersected with the row's own document, which is one contiguous run because
+            // the ids are non-decreasing (found once per tile, not per step); rows past N
+            // see every key (they are never stored)
+            int row_lo = 0, row_hi = p.N - 1;
             if (kMask && valid) {
                 if (p.window_left >= 0) row_lo = max(0, q_idx - p.window_left);
                 if (p.window_right >= 0) row_hi = min(row_hi, q_idx + p.window_right);
-                if (p.doc) my_doc = __ldg(p.doc + (size_t)(w.bh / p.H) * (size_t)p.N + q_idx);
+                if (p.doc) {
+                    const int* dseq = p.doc + (size_t)(w.bh / p.H) * (size_t)p.N;
+                    row_lo = max(row_lo, doc_first(dseq, q_idx));
+                    row_hi = min(row_hi, doc_last(dseq, q_idx, p.N));
+                }
             }
             float m_own = -INFINITY;  // reference this group's sums are relative to (base-2 units)
             float l_run = 0.f;        // this group's sum of bf16(2^(t - m_own)): normalises O
@@ -773,32 +779,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // keys this row may see in this tile: [first, last] (tile-relative);
                     // past the end of the sequence, outside the window (causal: past the
                     // diagonal) and outside the row's document are masked
-                    int first, last;
-                    {
-                        const int k0 = (w.j0 + j) * kBlockN;
-                        first = row_lo - k0;
-                        last = min(row_hi, p.N - 1) - k0;
-                        if (p.doc && valid) {
-                            const int* dk = p.doc + (size_t)(w.bh / p.H) * (size_t)p.N + k0;
-                            const int cnt = min(kBlockN, p.N - k0);
-                            if (__ldg(dk) != my_doc || __ldg(dk + cnt - 1) != my_doc) {
-                                // a document boundary falls in this tile: the row's keys are
-                                // the run of its own id (lower and upper bound)
-                                int a = 0, e = cnt;
-                                while (a < e) {
-                                    const int mid = (a + e) >> 1;
-                                    if (__ldg(dk + mid) < my_doc) a = mid + 1; else e = mid;
-                                }
-                                int b2 = a, e2 = cnt;
-                                while (b2 < e2) {
-                                    const int mid = (b2 + e2) >> 1;
-                                    if (__ldg(dk + mid) <= my_doc) b2 = mid + 1; else e2 = mid;
-                                }
-                                first = max(first, a);
-                                last = min(last, b2 - 1);
-                            }
-                        }
-                    }
+                    const int k0 = (w.j0 + j) * kBlockN;
+                    const int first = row_lo - k0;
+                    const int last = min(row_hi, p.N - 1) - k0;
                     if (first > 0 || last < kBlockN - 1) {
     #pragma unroll
                         for (int i = 0; i < kBlockN; ++i) s[i] = (i < first || i > last) ? -INFINITY : s[i];
