@@ -224,6 +224,20 @@ def test_output_alignment_and_bounds(fa, d):
     assert torch.all(buf[:pad + 8] == -7.0) and torch.all(buf[pad + 8 + n:] == -7.0)
 
 
+@pytest.mark.parametrize("B,H,N,d", [(1, 65535, 3, 64), (65535, 1, 40, 128)])
+def test_largest_head_count(fa, B, H, N, d):
+    """B*H at the limit the boundary accepts (65535): every (head, query tile)
+    unit runs through the persistent schedule's static rounds and dynamic tail;
+    sampled rows across the whole range, including the last head."""
+    w = wl.Workload("maxbh", B, H, N, d, True, "iid", 99)
+    q, k, v = wl.make_inputs(w)
+    o, lse = run_gpu(fa, q, k, v, True, w.scale)
+    rng = np.random.default_rng(100)
+    total = B * H * N
+    rows = np.unique(np.concatenate([rng.integers(0, total, 600), [0, N - 1, total - N, total - 1]])).astype(np.int64)
+    compare(o, lse, q, k, v, True, w.scale, rows, f"B{B} H{H} N{N} d{d}")
+
+
 def test_inputs_untouched(fa):
     w = wl.Workload("ro", 1, 2, 300, 64, False, "iid", 6)
     q, k, v = (t.cuda() for t in wl.make_inputs(w))

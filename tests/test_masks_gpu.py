@@ -107,6 +107,16 @@ def test_large_sliding_window_sampled_rows(fa):
     check(fa, B, H, N, d, 1023, 0, None, seed=10, rows=rows.astype(np.int64), label="N8192 window 1024")
 
 
+def test_documents_at_the_largest_batch(fa):
+    """B = 65535 sequences, each with its own document ids (the per-batch doc
+    offset at its largest), sampled rows including the last sequence."""
+    B, H, N, d = 65535, 1, 65, 64
+    docs = doc_ids(B, N, seed=21, mean_len=20)
+    rng = np.random.default_rng(22)
+    rows = np.unique(np.concatenate([rng.integers(0, B * H * N, 600), [0, B * H * N - 1]])).astype(np.int64)
+    check(fa, B, H, N, d, -1, 0, docs, seed=23, rows=rows, label="documents, B = 65535")
+
+
 def test_trivial_masks_equal_fa_fwd_bit_for_bit(fa):
     w = wl.Workload("eq", 1, 2, 777, 128, True, "iid", 12)
     q, k, v = (t.cuda() for t in wl.make_inputs(w))
