@@ -251,8 +251,11 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chu
  *                entry do not matter.
  *
  * Bf16 tensors 16-byte aligned; outputs and workspace must not overlap any
- * input or each other.  Three kernels are enqueued on `stream` (D, then dq,
- * then dk and dv).  Returns FA_OK, or FA_ERR_NULL_POINTER, FA_ERR_HEAD_DIM,
+ * input or each other.  Three kernels: D on `stream`, then dq on `stream` and,
+ * at the same time, dk and dv on an internal per-device stream (made on first
+ * use and kept).  Events order the dk/dv kernel after D, and the work enqueued
+ * on `stream` afterwards after both.  The enqueue of concurrent fa_bwd calls on
+ * one device is serialised by a lock.  Returns FA_OK, or FA_ERR_NULL_POINTER, FA_ERR_HEAD_DIM,
  * FA_ERR_SHAPE, FA_ERR_ALIGNMENT, FA_ERR_SCALE, FA_ERR_WORKSPACE,
  * FA_ERR_ALIAS, FA_ERR_DEVICE, FA_ERR_TENSOR_MAP, FA_ERR_CUDA.
  */

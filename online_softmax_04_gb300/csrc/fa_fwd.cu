@@ -245,6 +245,33 @@ int queue_slot(unsigned int** out) {
     return FA_OK;
 }
 
+// The backward's second stream and its two events, per device, made on first
+// use and kept; the enqueue of concurrent fa_bwd calls on one device is
+// serialised because they share them.
+struct BwdPipe {
+    bool ready = false;
+    cudaStream_t side = nullptr;
+    cudaEvent_t delta_done = nullptr, kv_done = nullptr;
+};
+BwdPipe g_bwd_pipe[kMaxDevices];
+std::mutex g_bwd_mu;
+
+int bwd_pipe(BwdPipe** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+    BwdPipe& bp = g_bwd_pipe[dev];
+    if (!bp.ready) {
+        if (cudaStreamCreateWithFlags(&bp.side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&bp.delta_done, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&bp.kv_done, cudaEventDisableTiming) != cudaSuccess)
+            return FA_ERR_CUDA;
+        bp.ready = true;
+    }
+    *out = &bp;
+    return FA_OK;
+}
+
 template <int D, int NS>
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                const void* o, const void* dout, float* delta, void* dq, void* dk, void* dv, fa::BwdParams p, int BH,
@@ -260,12 +287,24 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
         cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
         return FA_ERR_CUDA;
     const dim3 grid((unsigned)p.n_tiles, (unsigned)BH);
+    // dQ and dK/dV are independent once D is known: dK/dV runs on a second
+    // stream, so that each kernel's CTAs fill the other's last, partial wave
+    BwdPipe* bp = nullptr;
+    std::lock_guard<std::mutex> lk(g_bwd_mu);
+    const int prc = bwd_pipe(&bp);
+    if (prc != FA_OK) return prc;
+    if (cudaEventRecord(bp->delta_done, st) != cudaSuccess || cudaStreamWaitEvent(bp->side, bp->delta_done, 0) != cudaSuccess)
+        return FA_ERR_CUDA;
     p.delta = delta;
-    p.grad = dq;
-    kq<<<grid, fa::kBwdThreads, L::kAlloc, st>>>(tq, tk, tv, tdo, p);
     p.grad = dk;
     p.grad2 = dv;
-    kkv<<<grid, fa::kBwdThreads, L::kAlloc, st>>>(tq, tk, tv, tdo, p);
+    kkv<<<grid, fa::kBwdThreads, L::kAlloc, bp->side>>>(tq, tk, tv, tdo, p);
+    p.grad = dq;
+    p.grad2 = nullptr;
+    kq<<<grid, fa::kBwdThreads, L::kAlloc, st>>>(tq, tk, tv, tdo, p);
+    // the caller's stream continues once both have finished
+    if (cudaEventRecord(bp->kv_done, bp->side) != cudaSuccess || cudaStreamWaitEvent(st, bp->kv_done, 0) != cudaSuccess)
+        return FA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
