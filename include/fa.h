@@ -25,10 +25,13 @@
  *     lse        : fp32  [B][H][N]
  * Query and key sequences have the same length N.
  *
- * Ownership: every pointer is a DEVICE pointer owned by the caller.  The
- * library allocates nothing per call, keeps no reference after returning,
- * and never synchronises the host: the work is enqueued on `stream`
- * (0 = the legacy default stream) and completes asynchronously.
+ * Ownership: every pointer is a DEVICE pointer owned by the caller (except the
+ * tensors of fa_fwd_host, which are host pointers).  The library allocates no
+ * memory per call, keeps no reference after returning, and never synchronises
+ * the host: the work is enqueued on `stream` (0 = the legacy default stream)
+ * and completes asynchronously.  fa_fwd_host and fa_bwd also use internal
+ * per-device streams, made once and kept.  Events order that work with
+ * `stream` in both directions.
  *
  * Errors: each entry point returns FA_OK (0) or a negative FA_ERR_* code;
  * argument errors are detected on the host before anything is enqueued.
