@@ -498,20 +498,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float* stage = reinterpret_cast<float*>(smem + L::kOffStage) + (warp - 4) * 2 * 256;  // [2][LSE 128, D 128]
         const float c2 = p.scale_log2;
         bool ok = true;
-        for (int i = 0; i < n_q; ++i) {
-            const int qi = i0 + i;
-            // this query tile's -LSE (log2 units) and -D, staged once per warp; queries
-            // past N get -LSE = -inf, so their weights are 0
-            float* st = stage + (i & 1) * 256;
+        // LSE and D of query tile i0 + i into staging buffer i & 1, one step ahead,
+        // with cp.async (no registers held, no stall on the loads); queries past N
+        // read nothing
+        auto prefetch = [&](int i) {
+            const uint32_t sb = smem_u32(stage + (i & 1) * 256);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int c = u * 32 + lane;
-                const int q = qi * 128 + c;
-                const size_t r = (size_t)bh * p.N + (size_t)q;
-                st[c] = q < p.N ? -(p.lse[r] * kLog2e) : -INFINITY;
-                st[128 + c] = q < p.N ? -p.delta[r] : 0.f;
+                const int q = (i0 + i) * 128 + c;
+                const bool in = q < p.N;
+                const size_t r = (size_t)bh * p.N + (size_t)(in ? q : 0);
+                cp_async_4(sb + 4u * (uint32_t)c, p.lse + r, in ? 4u : 0u);
+                cp_async_4(sb + 4u * (uint32_t)(128 + c), p.delta + r, in ? 4u : 0u);
+            }
+        };
+        if (n_q > 0) prefetch(0);
+        for (int i = 0; i < n_q; ++i) {
+            const int qi = i0 + i;
+            // this query tile's -LSE (log2 units) and -D: each lane converts the entries
+            // it copied; queries past N get -LSE = -inf, so their weights are 0
+            float* st = stage + (i & 1) * 256;
+            cp_async_wait_all();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = u * 32 + lane;
+                const bool in = qi * 128 + c < p.N;
+                st[c] = in ? -(st[c] * kLog2e) : -INFINITY;
+                st[128 + c] = in ? -st[128 + c] : 0.f;
             }
             __syncwarp();
+            if (i + 1 < n_q) prefetch(i + 1);
             ok = fa_wait_warp(bar(L::kBarSFull), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
             if (!ok) break;
             tc_fence_after_sync();
@@ -571,6 +588,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kBarDSFull));
         }
+        cp_async_wait_all();  // after an abort a prefetch may still be in flight
         if (ok && n_q > 0) ok = fa_wait_warp(bar(L::kBarFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
         if (ok) {
             tc_fence_after_sync();

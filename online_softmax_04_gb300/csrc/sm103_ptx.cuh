@@ -59,6 +59,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // proxy (TMA, tensor-core operand reads)
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// 4-byte global -> shared copy that completes asynchronously (cp.async); with
+// src_bytes = 0 nothing is read and the destination is zero-filled
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// wait until every cp.async of this thread has completed
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), 3-D tiled
 // ----------------------------------------------------------------------------
