@@ -111,7 +111,9 @@ __device__ __forceinline__ void bwd_load_tile(uint32_t dst, const CUtensorMap* m
 
 // ---------------------------------------------------------------------------
 // dQ: one CTA per (query tile, head).  TMEM: S [0,128), dP [128,256),
-// dQ [256, 256+D), dS bf16 [256+D, 256+D+64).
+// dQ [256, 256+D), dS bf16 in two buffers [256+D, 256+D+64) and
+// [256+D+64, 256+D+128), alternating by step, so that dS(j) is formed while
+// the dQ product of dS(j-1) still reads the other buffer.
 // ---------------------------------------------------------------------------
 template <int D, int NS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const BwdParams p) {
     using L = BwdSmem<D, NS>;
     constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
+    static_assert(256 + D + 128 <= kTmemCols, "TMEM budget");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -141,7 +144,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(bar(L::kBarSFull), 1);
         mbar_init(bar(L::kBarDSFull), 8);
-        mbar_init(bar(L::kBarUsed), 1);
+        mbar_init(bar(L::kBarUsed + 0), 1);  // per dS buffer: its dQ product finished
+        mbar_init(bar(L::kBarUsed + 1), 1);
         mbar_init(bar(L::kBarFinal), 1);
         mbar_init(bar(L::kBarDrain), 1);
         mbar_init(bar(L::kBarDrain + 1), 1);
@@ -234,13 +238,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + kColDS + (uint32_t)kk * 8u,
+                    mma_ts(tmem + kColDQ, tmem + kColDS + 64u * (uint32_t)(j & 1) + (uint32_t)kk * 8u,
                            sdesc_sw128(ring_k(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescDQ,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 // S_j and dP_j finished before dS_j was written, so this covers every
                 // product that read stage s
                 tc_commit(bar(L::kBarEmpty + s));
-                tc_commit(bar(L::kBarUsed));
+                tc_commit(bar(L::kBarUsed + (j & 1)));
             }
             if (ok && n_kv > 0) tc_commit(bar(L::kBarFinal));
             tc_commit(bar(L::kBarDrain + 1));
@@ -272,9 +276,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kBarSRead));
-            // dS(j-1) must have been read by its dQ product before it is overwritten
-            if (j > 0)
-                ok = fa_wait_warp(bar(L::kBarUsed), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusSoftmaxWaitPV);
+            // dS buffer j & 1 last held dS(j-2): its dQ product must have read it
+            if (j >= 2)
+                ok = fa_wait_warp(bar(L::kBarUsed + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort_flag, limit,
+                                  kStatusSoftmaxWaitPV);
             if (!ok) break;
             tc_fence_after_sync();
             // keys visible to this row in this tile: c <= last
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             d1);
                         pk[i] = pack_bf16x2(d0, d1);
                     }
-                    tmem_st16(t_lane + kColDS + 16u * ch, pk);
+                    tmem_st16(t_lane + kColDS + 64u * (uint32_t)(j & 1) + 16u * ch, pk);
                 }
             } else {
 #pragma unroll
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         pk[i] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - drow),
                                             p1 * (__uint_as_float(dv[e + 1]) - drow));
                     }
-                    tmem_st16(t_lane + kColDS + 16u * ch, pk);
+                    tmem_st16(t_lane + kColDS + 64u * (uint32_t)(j & 1) + 16u * ch, pk);
                 }
             }
             tmem_st_wait();
