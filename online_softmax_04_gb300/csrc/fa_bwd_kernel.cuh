@@ -87,9 +87,10 @@ struct BwdSmem {
     static constexpr int kBarRes = 0;                   // resident tiles landed
     static constexpr int kBarFull = 1;                  // [NS] stage landed
     static constexpr int kBarEmpty = kBarFull + NS;     // [NS] stage consumed by the MMAs
-    static constexpr int kBarSFull = kBarEmpty + NS;    // the two score-like products of a step finished
-    static constexpr int kBarDSFull = kBarSFull + 1;    // compute warps wrote the bf16 operand(s)
-    static constexpr int kBarUsed = kBarDSFull + 1;     // [2] the products reading those operands finished
+    // [2] each: the dQ kernel uses index 0; the dK/dV kernel one per issuer (S / dV, dP / dK)
+    static constexpr int kBarSFull = kBarEmpty + NS;    // score-like product(s) of a step finished
+    static constexpr int kBarDSFull = kBarSFull + 2;    // compute warps wrote the bf16 operand(s)
+    static constexpr int kBarUsed = kBarDSFull + 2;     // the products reading those operands finished
     static constexpr int kBarFinal = kBarUsed + 2;      // the accumulators are complete
     static constexpr int kBarDrain = kBarFinal + 1;     // [2] per MMA issuer
     static constexpr int kBarSRead = kBarDrain + 2;     // dQ kernel: the compute warps hold S and dP in registers
@@ -393,8 +394,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar(L::kBarFull + s), 1);
             mbar_init(bar(L::kBarEmpty + s), 2);  // both issuers' products read the stage
         }
-        mbar_init(bar(L::kBarSFull), 2);  // both issuers
-        mbar_init(bar(L::kBarDSFull), 8);
+        mbar_init(bar(L::kBarSFull + 0), 1);   // S^T (warp 1)
+        mbar_init(bar(L::kBarSFull + 1), 1);   // dP^T (warp 3)
+        mbar_init(bar(L::kBarDSFull + 0), 8);  // P^T written
+        mbar_init(bar(L::kBarDSFull + 1), 8);  // dS^T written
         mbar_init(bar(L::kBarUsed + 0), 1);  // dV products (warp 1)
         mbar_init(bar(L::kBarUsed + 1), 1);  // dK products (warp 3)
         mbar_init(bar(L::kBarFinal), 2);
@@ -473,8 +476,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss(tmem + col_sc, sdesc_sw128(res_a + off, 16, 1024), sdesc_sw128(b_sc + off, 16, 1024), kIdescS,
                            kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(L::kBarSFull));
-                ok = fa_wait(bar(L::kBarDSFull), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
+                tc_commit(bar(L::kBarSFull + u));
+                // its bf16 operand: P^T (written first) or dS^T
+                ok = fa_wait(bar(L::kBarDSFull + u), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
                 if (!ok) break;
                 tc_fence_after_sync();
                 // the bf16 operands of queries 16 kk .. 16 kk + 15 sit at column
@@ -534,64 +538,82 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             __syncwarp();
             if (i + 1 < n_q) prefetch(i + 1);
-            ok = fa_wait_warp(bar(L::kBarSFull), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
-            if (!ok) break;
-            tc_fence_after_sync();
             // causal: query q sees key k_idx iff k_idx <= q, i.e. column c >= first
             // (only the diagonal tile masks; queries past N weigh 0 through -LSE)
             const bool diag = p.causal && qi == kt;
             const int first = diag ? row : 0;
             const uint64_t c2x2 = f32x2_pack(c2, c2);
+            // P^T and dS^T of query columns [64 half, +64) go to columns [64 half,
+            // 64 half + 32): inside what this warp has already read (64 half + 16 hc +
+            // 16 <= 64 half + 32 hc + 32), never into the other half's columns.
+            // Phase 1, as soon as S^T is in: P, stored as bf16 for the dV product
+            // (which starts at once) and kept in fp32 for dS.
+            ok = fa_wait_warp(bar(L::kBarSFull + 0), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            if (!ok) break;
+            tc_fence_after_sync();
+            float pf[64];
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
                 const int ch = 2 * half + hc;
-                uint32_t sv[32], dv[32], pk[16], dk[16];
+                uint32_t sv[32], pk[16];
                 tmem_ld32_wait(t_lane + kColS + 32u * ch, sv);
-                tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
                 if (!diag) {
-                    // packed fp32x2 arithmetic; -LSE and -D of two queries per load
+                    // packed fp32x2 arithmetic; -LSE of two queries per load
 #pragma unroll
                     for (int i2 = 0; i2 < 16; ++i2) {
                         const int c0 = 32 * ch + 2 * i2;
                         const float2 nl = *reinterpret_cast<const float2*>(st + c0);
-                        const float2 nd = *reinterpret_cast<const float2*>(st + 128 + c0);
                         float x0, x1;
                         f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(sv[2 * i2]), __uint_as_float(sv[2 * i2 + 1])),
                                            c2x2, f32x2_pack(nl.x, nl.y)),
                                      x0, x1);
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        pk[i2] = pack_bf16x2(p0, p1);
-                        float d0, d1;
-                        f32x2_unpack(fmul2(f32x2_pack(p0, p1),
-                                           fadd2(f32x2_pack(__uint_as_float(dv[2 * i2]), __uint_as_float(dv[2 * i2 + 1])),
-                                                 f32x2_pack(nd.x, nd.y))),
-                                     d0, d1);
-                        dk[i2] = pack_bf16x2(d0, d1);
+                        pf[32 * hc + 2 * i2] = ex2_approx(x0);
+                        pf[32 * hc + 2 * i2 + 1] = ex2_approx(x1);
                     }
                 } else {
 #pragma unroll
                     for (int i2 = 0; i2 < 16; ++i2) {
                         const int c0 = 32 * ch + 2 * i2;
-                        const float p0 =
+                        pf[32 * hc + 2 * i2] =
                             (c0 >= first) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i2]), c2, st[c0])) : 0.f;
-                        const float p1 =
+                        pf[32 * hc + 2 * i2 + 1] =
                             (c0 + 1 >= first) ? ex2_approx(fmaf(__uint_as_float(sv[2 * i2 + 1]), c2, st[c0 + 1])) : 0.f;
-                        pk[i2] = pack_bf16x2(p0, p1);
-                        dk[i2] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * i2]) + st[128 + c0]),
-                                             p1 * (__uint_as_float(dv[2 * i2 + 1]) + st[128 + c0 + 1]));
                     }
                 }
-                // P^T and dS^T of query columns [64 half, +64) go to columns
-                // [64 half, 64 half + 32): inside what this warp has already read
-                // (64 half + 16 hc + 16 <= 64 half + 32 hc + 32), never into the other
-                // half's columns
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) pk[i2] = pack_bf16x2(pf[32 * hc + 2 * i2], pf[32 * hc + 2 * i2 + 1]);
                 tmem_st16(t_lane + kColS + 64u * half + 16u * hc, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarDSFull + 0));
+            // Phase 2, once dP^T is in: dS = P (dP - D), for the dK product
+            ok = fa_wait_warp(bar(L::kBarSFull + 1), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            if (!ok) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                const int ch = 2 * half + hc;
+                uint32_t dv[32], dk[16];
+                tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    const int c0 = 32 * ch + 2 * i2;
+                    const float2 nd = *reinterpret_cast<const float2*>(st + 128 + c0);
+                    float d0, d1;
+                    f32x2_unpack(fmul2(f32x2_pack(pf[32 * hc + 2 * i2], pf[32 * hc + 2 * i2 + 1]),
+                                       fadd2(f32x2_pack(__uint_as_float(dv[2 * i2]), __uint_as_float(dv[2 * i2 + 1])),
+                                             f32x2_pack(nd.x, nd.y))),
+                                 d0, d1);
+                    dk[i2] = pack_bf16x2(d0, d1);
+                }
                 tmem_st16(t_lane + kColDP + 64u * half + 16u * hc, dk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarDSFull));
+            if (lane == 0) mbar_arrive(bar(L::kBarDSFull + 1));
         }
         cp_async_wait_all();  // after an abort a prefetch may still be in flight
         if (ok && n_q > 0) ok = fa_wait_warp(bar(L::kBarFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
