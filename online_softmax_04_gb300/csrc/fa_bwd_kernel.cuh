@@ -87,14 +87,15 @@ struct BwdSmem {
     static constexpr int kBarRes = 0;                   // resident tiles landed
     static constexpr int kBarFull = 1;                  // [NS] stage landed
     static constexpr int kBarEmpty = kBarFull + NS;     // [NS] stage consumed by the MMAs
-    // [2] each: the dQ kernel uses index 0; the dK/dV kernel one per issuer (S / dV, dP / dK)
-    static constexpr int kBarSFull = kBarEmpty + NS;    // score-like product(s) of a step finished
+    // [2] each: SFull per score-like product (S, dP); DSFull and Used per dK/dV issuer in
+    // the dK/dV kernel, Used per dS buffer in the dQ kernel
+    static constexpr int kBarSFull = kBarEmpty + NS;    // score-like product of a step finished
     static constexpr int kBarDSFull = kBarSFull + 2;    // compute warps wrote the bf16 operand(s)
     static constexpr int kBarUsed = kBarDSFull + 2;     // the products reading those operands finished
     static constexpr int kBarFinal = kBarUsed + 2;      // the accumulators are complete
     static constexpr int kBarDrain = kBarFinal + 1;     // [2] per MMA issuer
-    static constexpr int kBarSRead = kBarDrain + 2;     // dQ kernel: the compute warps hold S and dP in registers
-    static constexpr int kNumBars = kBarSRead + 1;
+    static constexpr int kBarSRead = kBarDrain + 2;     // [2] dQ kernel: the compute warps hold S / dP in registers
+    static constexpr int kNumBars = kBarSRead + 2;
     static constexpr uint32_t kOffStage = kOffBar + kNumBars * 8;     // [8 warps][2][LSE 128, D 128] floats
     static constexpr uint32_t kOffTmemSlot = kOffStage + 8 * 2 * 256 * 4;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
@@ -143,14 +144,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar(L::kBarFull + s), 1);
             mbar_init(bar(L::kBarEmpty + s), 1);
         }
-        mbar_init(bar(L::kBarSFull), 1);
+        mbar_init(bar(L::kBarSFull + 0), 1);  // S
+        mbar_init(bar(L::kBarSFull + 1), 1);  // dP
         mbar_init(bar(L::kBarDSFull), 8);
         mbar_init(bar(L::kBarUsed + 0), 1);  // per dS buffer: its dQ product finished
         mbar_init(bar(L::kBarUsed + 1), 1);
         mbar_init(bar(L::kBarFinal), 1);
         mbar_init(bar(L::kBarDrain), 1);
         mbar_init(bar(L::kBarDrain + 1), 1);
-        mbar_init(bar(L::kBarSRead), 8);
+        mbar_init(bar(L::kBarSRead + 0), 8);  // S in registers
+        mbar_init(bar(L::kBarSRead + 1), 8);  // dP in registers
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_q);
@@ -195,8 +198,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // score products: S_j = Q K_j^T and dP_j = dO V_j^T, as soon as K_j, V_j
-        // have landed and the compute warps hold S_{j-1}, dP_{j-1} in registers
+        // score products: S_j = Q K_j^T and then dP_j = dO V_j^T, each as soon as
+        // K_j, V_j have landed and the compute warps hold S_{j-1} (resp. dP_{j-1}) in
+        // registers; each is signalled on its own, so the compute warps start on S_j
+        // while dP_j is still being formed
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
             bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
@@ -204,7 +209,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int s = j % NS;
                 ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
                 if (ok && j > 0)
-                    ok = fa_wait(bar(L::kBarSRead), (uint32_t)((j - 1) & 1), abort_flag, limit, kStatusMmaWaitSFree);
+                    ok = fa_wait(bar(L::kBarSRead + 0), (uint32_t)((j - 1) & 1), abort_flag, limit,
+                                 kStatusMmaWaitSFree);
                 if (!ok) break;
                 tc_fence_after_sync();
 #pragma unroll
@@ -213,13 +219,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss(tmem + kColS, sdesc_sw128(res_q + off, 16, 1024), sdesc_sw128(ring_k(s) + off, 16, 1024),
                            kIdescS, kk > 0 ? 1u : 0u);
                 }
+                tc_commit(bar(L::kBarSFull + 0));
+                if (j > 0)
+                    ok = fa_wait(bar(L::kBarSRead + 1), (uint32_t)((j - 1) & 1), abort_flag, limit,
+                                 kStatusMmaWaitSFree);
+                if (!ok) break;
+                tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
                     mma_ss(tmem + kColDP, sdesc_sw128(res_do + off, 16, 1024),
                            sdesc_sw128(ring_v(s) + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(L::kBarSFull));
+                tc_commit(bar(L::kBarSFull + 1));
             }
             tc_commit(bar(L::kBarDrain));
             fa_wait_drain(bar(L::kBarDrain), 0, limit);
@@ -266,31 +278,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float c2 = p.scale_log2;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            ok = fa_wait_warp(bar(L::kBarSFull), (uint32_t)(j & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            // Phase 1, as soon as S_j is in: P in place of S (fp32 bits), while dP_j
+            // is still being formed
+            ok = fa_wait_warp(bar(L::kBarSFull + 0), (uint32_t)(j & 1), abort_flag, limit, kStatusSoftmaxWaitS);
             if (!ok) break;
             tc_fence_after_sync();
-            // this warp's 64 columns of S and dP into registers, then release the
-            // columns to the next step's products
             uint32_t sv[64], dv[64];
             tmem_ld64_wait(t_lane + kColS + 64u * half, sv);
-            tmem_ld64_wait(t_lane + kColDP + 64u * half, dv);
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarSRead));
-            // dS buffer j & 1 last held dS(j-2): its dQ product must have read it
-            if (j >= 2)
-                ok = fa_wait_warp(bar(L::kBarUsed + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort_flag, limit,
-                                  kStatusSoftmaxWaitPV);
-            if (!ok) break;
-            tc_fence_after_sync();
+            if (lane == 0) mbar_arrive(bar(L::kBarSRead + 0));  // S columns free for S_{j+1}
             // keys visible to this row in this tile: c <= last
             int last = p.N - 1 - j * 128;
             if (p.causal && j == qt) last = min(last, row);
             if (__all_sync(0xffffffffu, last >= 127)) {
                 // every key of the tile visible to every row of the warp: packed
                 // fp32x2 arithmetic, no masks
-                const uint64_t c2x2 = f32x2_pack(c2, c2), nl2 = f32x2_pack(-lse2, -lse2),
-                               nd2 = f32x2_pack(-drow, -drow);
+                const uint64_t c2x2 = f32x2_pack(c2, c2), nl2 = f32x2_pack(-lse2, -lse2);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x0, x1;
+                    f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), c2x2, nl2),
+                                 x0, x1);
+                    sv[2 * i] = __float_as_uint(ex2_approx(x0));
+                    sv[2 * i + 1] = __float_as_uint(ex2_approx(x1));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const int c = 64 * half + e;
+                    sv[e] = __float_as_uint((c <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e]), c2, -lse2)) : 0.f);
+                }
+            }
+            // Phase 2, once dP_j is in: dS = P (dP - D) into dS buffer j & 1
+            ok = fa_wait_warp(bar(L::kBarSFull + 1), (uint32_t)(j & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            if (!ok) break;
+            tc_fence_after_sync();
+            tmem_ld64_wait(t_lane + kColDP + 64u * half, dv);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarSRead + 1));  // dP columns free for dP_{j+1}
+            // dS buffer j & 1 last held dS(j-2): its dQ product must have read it
+            if (j >= 2)
+                ok = fa_wait_warp(bar(L::kBarUsed + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort_flag, limit,
+                                  kStatusSoftmaxWaitPV);
+            if (!ok) break;
+            tc_fence_after_sync();
+            {
+                const uint64_t nd2 = f32x2_pack(-drow, -drow);
 #pragma unroll
                 for (int hc = 0; hc < 2; ++hc) {
                     const int ch = 2 * half + hc;
@@ -298,31 +333,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int e = 32 * hc + 2 * i;
-                        float x0, x1;
-                        f32x2_unpack(ffma2(f32x2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, nl2),
-                                     x0, x1);
-                        const uint64_t pp = f32x2_pack(ex2_approx(x0), ex2_approx(x1));
                         float d0, d1;
-                        f32x2_unpack(
-                            fmul2(pp, fadd2(f32x2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)), d0,
-                            d1);
+                        f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                           fadd2(f32x2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)),
+                                     d0, d1);
                         pk[i] = pack_bf16x2(d0, d1);
-                    }
-                    tmem_st16(t_lane + kColDS + 64u * (uint32_t)(j & 1) + 16u * ch, pk);
-                }
-            } else {
-#pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {
-                    const int ch = 2 * half + hc;
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int c0 = 32 * ch + 2 * i, e = 32 * hc + 2 * i;
-                        const float p0 = (c0 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e]), c2, -lse2)) : 0.f;
-                        const float p1 =
-                            (c0 + 1 <= last) ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), c2, -lse2)) : 0.f;
-                        pk[i] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - drow),
-                                            p1 * (__uint_as_float(dv[e + 1]) - drow));
                     }
                     tmem_st16(t_lane + kColDS + 64u * (uint32_t)(j & 1) + 16u * ch, pk);
                 }
