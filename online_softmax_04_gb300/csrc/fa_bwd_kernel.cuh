@@ -174,23 +174,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto ring_v = [&](int s) { return sbase + L::kOffRing + (uint32_t)(2 * s + 1) * L::kTileBytes; };
 
     if (warp == 0) {
-        if (lane == 0) {
+        // the whole warp walks the loop; one elected lane issues the copies
+        {
             bool ok = true;
-            mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
-            bwd_load_tile<D>(res_q, &tm_q, bar(L::kBarRes), qt * 128, bh);
-            bwd_load_tile<D>(res_do, &tm_do, bar(L::kBarRes), qt * 128, bh);
+            if (elect_one_sync()) {
+                mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
+                bwd_load_tile<D>(res_q, &tm_q, bar(L::kBarRes), qt * 128, bh);
+                bwd_load_tile<D>(res_do, &tm_do, bar(L::kBarRes), qt * 128, bh);
+            }
+            __syncwarp();
             int j = 0;
             for (; ok && j < n_kv; ++j) {
                 const int s = j % NS;
                 if (j >= NS)
-                    ok = fa_wait(bar(L::kBarEmpty + s), (uint32_t)(((j - NS) / NS) & 1), abort_flag, limit,
-                                 kStatusLoadWait);
+                    ok = fa_wait_warp(bar(L::kBarEmpty + s), (uint32_t)(((j - NS) / NS) & 1), abort_flag, limit,
+                                      kStatusLoadWait);
                 if (!ok) break;
-                mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
-                bwd_load_tile<D>(ring_k(s), &tm_k, bar(L::kBarFull + s), j * 128, bh);
-                bwd_load_tile<D>(ring_v(s), &tm_v, bar(L::kBarFull + s), j * 128, bh);
+                if (elect_one_sync()) {
+                    mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
+                    bwd_load_tile<D>(ring_k(s), &tm_k, bar(L::kBarFull + s), j * 128, bh);
+                    bwd_load_tile<D>(ring_v(s), &tm_v, bar(L::kBarFull + s), j * 128, bh);
+                }
+                __syncwarp();
             }
-            if (!ok || *abort_flag) {  // let every issued copy land before the CTA exits
+            if (lane == 0 && (!ok || *abort_flag)) {  // let every issued copy land before the CTA exits
                 fa_wait_drain(bar(L::kBarRes), 0, limit);
                 for (int s = 0; s < NS; ++s)
                     if (j > s) fa_wait_drain(bar(L::kBarFull + s), (uint32_t)(((j - 1 - s) / NS) & 1), limit);
@@ -202,66 +209,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // K_j, V_j have landed and the compute warps hold S_{j-1} (resp. dP_{j-1}) in
         // registers; each is signalled on its own, so the compute warps start on S_j
         // while dP_j is still being formed
-        if (lane == 0) {
+        {
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
-            bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
+            const uint64_t qd = sdesc_sw128(res_q, 16, 1024), dod = sdesc_sw128(res_do, 16, 1024);
+            bool ok = fa_wait_warp(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int s = j % NS;
-                ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
+                ok = fa_wait_warp(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
                 if (ok && j > 0)
-                    ok = fa_wait(bar(L::kBarSRead + 0), (uint32_t)((j - 1) & 1), abort_flag, limit,
-                                 kStatusMmaWaitSFree);
+                    ok = fa_wait_warp(bar(L::kBarSRead + 0), (uint32_t)((j - 1) & 1), abort_flag, limit,
+                                      kStatusMmaWaitSFree);
                 if (!ok) break;
                 tc_fence_after_sync();
+                const uint64_t kd = sdesc_sw128(ring_k(s), 16, 1024), vd = sdesc_sw128(ring_v(s), 16, 1024);
+                if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + kColS, sdesc_sw128(res_q + off, 16, 1024), sdesc_sw128(ring_k(s) + off, 16, 1024),
-                           kIdescS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                        mma_ss(tmem + kColS, sdesc_add_lo(qd, off), sdesc_add_lo(kd, off), kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::kBarSFull + 0));
                 }
-                tc_commit(bar(L::kBarSFull + 0));
+                __syncwarp();
                 if (j > 0)
-                    ok = fa_wait(bar(L::kBarSRead + 1), (uint32_t)((j - 1) & 1), abort_flag, limit,
-                                 kStatusMmaWaitSFree);
+                    ok = fa_wait_warp(bar(L::kBarSRead + 1), (uint32_t)((j - 1) & 1), abort_flag, limit,
+                                      kStatusMmaWaitSFree);
                 if (!ok) break;
                 tc_fence_after_sync();
+                if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + kColDP, sdesc_sw128(res_do + off, 16, 1024),
-                           sdesc_sw128(ring_v(s) + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                        mma_ss(tmem + kColDP, sdesc_add_lo(dod, off), sdesc_add_lo(vd, off), kIdescS,
+                               kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::kBarSFull + 1));
                 }
-                tc_commit(bar(L::kBarSFull + 1));
+                __syncwarp();
             }
-            tc_commit(bar(L::kBarDrain));
-            fa_wait_drain(bar(L::kBarDrain), 0, limit);
+            if (elect_one_sync()) {
+                tc_commit(bar(L::kBarDrain));
+                fa_wait_drain(bar(L::kBarDrain), 0, limit);
+            }
         }
         __syncwarp();
     } else if (warp == 3) {
         // gradient products, on a second issuing thread so that they overlap the
         // next step's score products: dQ += dS_j K_j once dS_j is in TMEM
-        if (lane == 0) {
+        {
             constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, false, true);
-            bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
+            bool ok = fa_wait_warp(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int s = j % NS;
-                ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK) &&
-                     fa_wait(bar(L::kBarDSFull), (uint32_t)(j & 1), abort_flag, limit, kStatusMmaWaitP);
+                ok = fa_wait_warp(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit,
+                                  kStatusMmaWaitK) &&
+                     fa_wait_warp(bar(L::kBarDSFull), (uint32_t)(j & 1), abort_flag, limit, kStatusMmaWaitP);
                 if (!ok) break;
                 tc_fence_after_sync();
+                const uint64_t kd = sdesc_sw128(ring_k(s), kChunkBytes, 1024);  // + 2048 bytes per 16 keys
+                if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + kColDS + 64u * (uint32_t)(j & 1) + (uint32_t)kk * 8u,
-                           sdesc_sw128(ring_k(s) + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescDQ,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                // S_j and dP_j finished before dS_j was written, so this covers every
-                // product that read stage s
-                tc_commit(bar(L::kBarEmpty + s));
-                tc_commit(bar(L::kBarUsed + (j & 1)));
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + kColDQ, tmem + kColDS + 64u * (uint32_t)(j & 1) + (uint32_t)kk * 8u,
+                               sdesc_add_lo(kd, (uint32_t)kk * 128u), kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
+                    // S_j and dP_j finished before dS_j was written, so this covers every
+                    // product that read stage s
+                    tc_commit(bar(L::kBarEmpty + s));
+                    tc_commit(bar(L::kBarUsed + (j & 1)));
+                }
+                __syncwarp();
             }
-            if (ok && n_kv > 0) tc_commit(bar(L::kBarFinal));
-            tc_commit(bar(L::kBarDrain + 1));
-            fa_wait_drain(bar(L::kBarDrain + 1), 0, limit);
+            if (elect_one_sync()) {
+                if (ok && n_kv > 0) tc_commit(bar(L::kBarFinal));
+                tc_commit(bar(L::kBarDrain + 1));
+                fa_wait_drain(bar(L::kBarDrain + 1), 0, limit);
+            }
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -438,23 +460,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto ring_do = [&](int s) { return sbase + L::kOffRing + (uint32_t)(2 * s + 1) * L::kTileBytes; };
 
     if (warp == 0) {
-        if (lane == 0) {
+        {
             bool ok = true;
-            mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
-            bwd_load_tile<D>(res_k, &tm_k, bar(L::kBarRes), kt * 128, bh);
-            bwd_load_tile<D>(res_v, &tm_v, bar(L::kBarRes), kt * 128, bh);
+            if (elect_one_sync()) {
+                mbar_arrive_expect_tx(bar(L::kBarRes), 2 * L::kTileBytes);
+                bwd_load_tile<D>(res_k, &tm_k, bar(L::kBarRes), kt * 128, bh);
+                bwd_load_tile<D>(res_v, &tm_v, bar(L::kBarRes), kt * 128, bh);
+            }
+            __syncwarp();
             int i = 0;
             for (; ok && i < n_q; ++i) {
                 const int s = i % NS;
                 if (i >= NS)
-                    ok = fa_wait(bar(L::kBarEmpty + s), (uint32_t)(((i - NS) / NS) & 1), abort_flag, limit,
-                                 kStatusLoadWait);
+                    ok = fa_wait_warp(bar(L::kBarEmpty + s), (uint32_t)(((i - NS) / NS) & 1), abort_flag, limit,
+                                      kStatusLoadWait);
                 if (!ok) break;
-                mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
-                bwd_load_tile<D>(ring_q(s), &tm_q, bar(L::kBarFull + s), (i0 + i) * 128, bh);
-                bwd_load_tile<D>(ring_do(s), &tm_do, bar(L::kBarFull + s), (i0 + i) * 128, bh);
+                if (elect_one_sync()) {
+                    mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
+                    bwd_load_tile<D>(ring_q(s), &tm_q, bar(L::kBarFull + s), (i0 + i) * 128, bh);
+                    bwd_load_tile<D>(ring_do(s), &tm_do, bar(L::kBarFull + s), (i0 + i) * 128, bh);
+                }
+                __syncwarp();
             }
-            if (!ok || *abort_flag) {
+            if (lane == 0 && (!ok || *abort_flag)) {
                 fa_wait_drain(bar(L::kBarRes), 0, limit);
                 for (int s = 0; s < NS; ++s)
                     if (i > s) fa_wait_drain(bar(L::kBarFull + s), (uint32_t)(((i - 1 - s) / NS) & 1), limit);
@@ -466,50 +494,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // S^T = K Q_i^T and then dV += P^T dO_i, warp 3 issues dP^T = V dO_i^T and
         // then dK += dS^T Q_i.  Each thread's score product overwrites the columns
         // its own gradient product of step i-1 read, so it waits for that product.
-        if (lane == 0) {
+        {
             const int u = warp == 1 ? 0 : 1;  // 0: S / dV, 1: dP / dK
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
             constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);
             const uint32_t res_a = u == 0 ? res_k : res_v;  // K for S^T, V for dP^T
             const uint32_t col_sc = u == 0 ? kColS : kColDP;
             const uint32_t col_acc = u == 0 ? kColDV : kColDK;
-            bool ok = fa_wait(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
+            const uint64_t ad = sdesc_sw128(res_a, 16, 1024);
+            bool ok = fa_wait_warp(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
             for (int i = 0; ok && i < n_q; ++i) {
                 const int s = i % NS;
                 const uint32_t b_sc = u == 0 ? ring_q(s) : ring_do(s);   // B of the score product
                 const uint32_t b_acc = u == 0 ? ring_do(s) : ring_q(s);  // B of the gradient product
-                ok = fa_wait(bar(L::kBarFull + s), (uint32_t)((i / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
+                ok = fa_wait_warp(bar(L::kBarFull + s), (uint32_t)((i / NS) & 1), abort_flag, limit,
+                                  kStatusMmaWaitK);
                 // this thread's score columns hold its bf16 operand of step i-1 until its
                 // gradient product has finished
                 if (ok && i > 0)
-                    ok = fa_wait(bar(L::kBarUsed + u), (uint32_t)((i - 1) & 1), abort_flag, limit, kStatusMmaWaitSFree);
+                    ok = fa_wait_warp(bar(L::kBarUsed + u), (uint32_t)((i - 1) & 1), abort_flag, limit,
+                                      kStatusMmaWaitSFree);
                 if (!ok) break;
                 tc_fence_after_sync();
+                const uint64_t bd = sdesc_sw128(b_sc, 16, 1024);
+                if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tmem + col_sc, sdesc_sw128(res_a + off, 16, 1024), sdesc_sw128(b_sc + off, 16, 1024), kIdescS,
-                           kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                        mma_ss(tmem + col_sc, sdesc_add_lo(ad, off), sdesc_add_lo(bd, off), kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::kBarSFull + u));
                 }
-                tc_commit(bar(L::kBarSFull + u));
+                __syncwarp();
                 // its bf16 operand: P^T (written first) or dS^T
-                ok = fa_wait(bar(L::kBarDSFull + u), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
+                ok = fa_wait_warp(bar(L::kBarDSFull + u), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
                 if (!ok) break;
                 tc_fence_after_sync();
                 // the bf16 operands of queries 16 kk .. 16 kk + 15 sit at column
-                // 8 kk (first half of the queries) or 32 + 8 kk (second half)
+                // 8 kk (first half of the queries) or 32 + 8 kk (second half); the B rows
+                // advance 2048 bytes per 16 queries
+                const uint64_t gd = sdesc_sw128(b_acc, kChunkBytes, 1024);
+                if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    mma_ts(tmem + col_acc, tmem + col_sc + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
-                           sdesc_sw128(b_acc + (uint32_t)kk * 2048u, kChunkBytes, 1024), kIdescG,
-                           (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + col_acc, tmem + col_sc + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
+                               sdesc_add_lo(gd, (uint32_t)kk * 128u), kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar(L::kBarEmpty + s));
+                    tc_commit(bar(L::kBarUsed + u));
                 }
-                tc_commit(bar(L::kBarEmpty + s));
-                tc_commit(bar(L::kBarUsed + u));
+                __syncwarp();
             }
-            if (ok && n_q > 0) tc_commit(bar(L::kBarFinal));
-            tc_commit(bar(L::kBarDrain + u));
-            fa_wait_drain(bar(L::kBarDrain + u), 0, limit);
+            if (elect_one_sync()) {
+                if (ok && n_q > 0) tc_commit(bar(L::kBarFinal));
+                tc_commit(bar(L::kBarDrain + u));
+                fa_wait_drain(bar(L::kBarDrain + u), 0, limit);
+            }
         }
         __syncwarp();
     } else if (warp >= 4) {

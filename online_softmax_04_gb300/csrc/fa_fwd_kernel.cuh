@@ -154,6 +154,9 @@ struct FaSmem {
     static constexpr int kBarQ = 0;  // per Q buffer: the tile landed
     static constexpr int kBarKFull = kBarQ + kQBufs;
     static constexpr int kBarKEmpty = kBarKFull + NK;
+    // with two K stages, stage g % 2 is free once S_g (buffer g % 2) has finished:
+    // the producer then waits on SFull and the S issuer commits one barrier a step
+    static constexpr bool kKEmptyIsSFull = NK == 2;
     static constexpr int kBarVFull = kBarKEmpty + NK;
     static constexpr int kBarVEmpty = kBarVFull + NV;
     static constexpr int kBarSFull = kBarVEmpty + NV;  // per S buffer: S_j written
@@ -541,7 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_k = [&](const TileWork& w, int j) -> bool {
                 const int s = nk % NK;
                 const uint32_t r = (uint32_t)(nk / NK);
-                if (!fa_wait(bar(L::kBarKEmpty + s), (r & 1u) ^ 1u, abort_flag, limit, kStatusLoadWait)) return false;
+                const uint32_t empty = bar((L::kKEmptyIsSFull ? L::kBarSFull : L::kBarKEmpty) + s);
+                if (!fa_wait(empty, (r & 1u) ^ 1u, abort_flag, limit, kStatusLoadWait)) return false;
                 mbar_arrive_expect_tx(bar(L::kBarKFull + s), L::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
@@ -605,42 +609,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_{g-2} out of that buffer.  After a tile's last S: commit QFree of
         // its Q buffer.
         // ------------------------------------------------------------------
-        if (lane == 0) {
+        {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
             int g = 0, t = 0;
             Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
             TileWork w;
             bool ok = true;
-            while (ok && seq.template next<false>(p, w)) {
+            while (ok && seq.template next<true>(p, w)) {
                 if (w.n_kv == 0) continue;
                 const int qb = t % L::kQBufs;
                 const uint32_t qa = sbase + L::kOffQ + (uint32_t)qb * L::kTileBytes;
-                ok = fa_wait(bar(L::kBarQ + qb), (uint32_t)((t / L::kQBufs) & 1), abort_flag, limit, kStatusMmaWaitQ);
+                ok = fa_wait_warp(bar(L::kBarQ + qb), (uint32_t)((t / L::kQBufs) & 1), abort_flag, limit,
+                                  kStatusMmaWaitQ);
                 for (int j = 0; ok && j < w.n_kv; ++j, ++g) {
                     const int b = g & 1;
                     const int ks = g % NK;
                     if (g >= 2)
-                        ok = fa_wait(bar(L::kBarSFree + b), (uint32_t)(((g - 2) >> 1) & 1), abort_flag, limit,
-                                     kStatusMmaWaitSFree);
-                    ok = ok && fa_wait(bar(L::kBarKFull + ks), (uint32_t)((g / NK) & 1), abort_flag, limit,
-                                       kStatusMmaWaitK);
+                        ok = fa_wait_warp(bar(L::kBarSFree + b), (uint32_t)(((g - 2) >> 1) & 1), abort_flag, limit,
+                                          kStatusMmaWaitSFree);
+                    ok = ok && fa_wait_warp(bar(L::kBarKFull + ks), (uint32_t)((g / NK) & 1), abort_flag, limit,
+                                            kStatusMmaWaitK);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t ka = sbase + L::kOffK + (uint32_t)ks * L::kTileBytes;
+                    // descriptors built once; K step kk moves the start address (16-byte
+                    // units, the low field) by its byte offset
+                    const uint64_t qd = sdesc_sw128(qa, 16, 1024), kd = sdesc_sw128(ka, 16, 1024);
+                    if (elect_one_sync()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u;
-                        mma_ss(tmem + L::col_s(b), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                               kIdescS, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = ((uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                            mma_ss(tmem + L::col_s(b), sdesc_add_lo(qd, off), sdesc_add_lo(kd, off), kIdescS,
+                                   kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::kBarSFull + b));
+                        if constexpr (!L::kKEmptyIsSFull) tc_commit(bar(L::kBarKEmpty + ks));
                     }
-                    tc_commit(bar(L::kBarSFull + b));
-                    tc_commit(bar(L::kBarKEmpty + ks));
+                    __syncwarp();
                 }
-                if (ok) tc_commit(bar(L::kBarQFree + qb));  // the Q buffer may be refilled once these finish
+                if (ok && elect_one_sync()) tc_commit(bar(L::kBarQFree + qb));  // the Q buffer may be refilled once these finish
+                __syncwarp();
                 ++t;
             }
-            tc_commit(bar(L::kBarDrain + 0));  // every MMA must finish before TMEM is released
-            fa_wait_drain(bar(L::kBarDrain + 0), 0, limit);
+            if (elect_one_sync()) {
+                tc_commit(bar(L::kBarDrain + 0));  // every MMA must finish before TMEM is released
+                fa_wait_drain(bar(L::kBarDrain + 0), 0, limit);
+            }
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -649,43 +663,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first product of a tile (which overwrites O) also waits until the
         // softmax warps have read the previous tile's O out of TMEM.
         // ------------------------------------------------------------------
-        if (lane == 0) {
+        {
             constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D + L::kSumCols, false, true);
             int g = 0, t = 0;
             Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
             TileWork w;
             bool ok = true;
-            while (ok && seq.template next<false>(p, w)) {
+            while (ok && seq.template next<true>(p, w)) {
                 if (w.n_kv == 0) continue;
                 for (int j = 0; ok && j < w.n_kv; ++j, ++g) {
                     const int b = g & 1;
                     const int vs = g % NV;
-                    ok = fa_wait(bar(L::kBarPFull + b), (uint32_t)((g >> 1) & 1), abort_flag, limit,
-                                 kStatusMmaWaitP) &&
-                         fa_wait(bar(L::kBarVFull + vs), (uint32_t)((g / NV) & 1), abort_flag, limit,
-                                 kStatusMmaWaitV);
+                    ok = fa_wait_warp(bar(L::kBarPFull + b), (uint32_t)((g >> 1) & 1), abort_flag, limit,
+                                      kStatusMmaWaitP) &&
+                         fa_wait_warp(bar(L::kBarVFull + vs), (uint32_t)((g / NV) & 1), abort_flag, limit,
+                                      kStatusMmaWaitV);
                     if (ok && j == 0 && t > 0)
-                        ok = fa_wait(bar(L::kBarOFree), (uint32_t)((t - 1) & 1), abort_flag, limit, kStatusMmaWaitP);
+                        ok = fa_wait_warp(bar(L::kBarOFree), (uint32_t)((t - 1) & 1), abort_flag, limit,
+                                          kStatusMmaWaitP);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t va = sbase + L::kOffV + (uint32_t)vs * L::kTileBytes;
+                    // second 64-column block of B: the next chunk of V (d = 128), or the
+                    // ones tile for the row sums (d = 64), whose leading-byte offset from
+                    // key rows 16 kk .. 16 kk + 15 shrinks as those rows advance
+                    const uint64_t vd0 = sdesc_sw128(va, L::kTcSum ? sbase + L::kOffOnes - va : kChunkBytes, 1024);
+                    constexpr uint32_t kStepDesc = L::kTcSum ? 128u - (128u << 16) : 128u;  // 2048 bytes per K step
+                    if (elect_one_sync()) {
 #pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        const uint32_t vk = va + (uint32_t)kk * 2048u;  // key rows 16 kk .. 16 kk + 15
-                        // second 64-column block: the next chunk of V (d = 128), or the
-                        // ones tile for the row sums (d = 64)
-                        const uint32_t lbo = L::kTcSum ? sbase + L::kOffOnes - vk : kChunkBytes;
-                        mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u, sdesc_sw128(vk, lbo, 1024),
-                               kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kBlockN / 16; ++kk)
+                            mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u,
+                                   sdesc_add_lo(vd0, (uint32_t)kk * kStepDesc), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bar(L::kBarVEmpty + vs));
+                        tc_commit(bar(L::kBarPVDone + b));
+                        if (j + 1 == w.n_kv) tc_commit(bar(L::kBarOFinal));
                     }
-                    tc_commit(bar(L::kBarVEmpty + vs));
-                    tc_commit(bar(L::kBarPVDone + b));
-                    if (j + 1 == w.n_kv) tc_commit(bar(L::kBarOFinal));
+                    __syncwarp();
                 }
                 ++t;
             }
-            tc_commit(bar(L::kBarDrain + 1));
-            fa_wait_drain(bar(L::kBarDrain + 1), 0, limit);
+            if (elect_one_sync()) {
+                tc_commit(bar(L::kBarDrain + 1));
+                fa_wait_drain(bar(L::kBarDrain + 1), 0, limit);
+            }
         }
         __syncwarp();
     } else if (warp >= 4) {

@@ -163,6 +163,26 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// True in exactly one lane of the (fully converged) warp.  A converged warp
+// elects the same lane every time, so the tcgen05 products and the commits
+// that track them (a commit covers only its own thread's earlier operations)
+// can each sit in an elected block of their own.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
+// A descriptor with `add` added to its low word (start address and leading-byte
+// offset fields).  For callers whose field sums stay inside their fields, so that
+// no carry reaches the high word: one 32-bit add instead of a 64-bit one.
+__device__ __forceinline__ uint64_t sdesc_add_lo(uint64_t d, uint32_t add) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tadd.u32 lo, lo, %2;\n\tmov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(r) : "l"(d), "r"(add));
+    return r;
+}
+
 // ----------------------------------------------------------------------------
 // tcgen05.ld / tcgen05.st, shape 32x32b: lane t of the warp moves TMEM lane
 // (warp quarter * 32 + t), register i <-> column (col + i).
