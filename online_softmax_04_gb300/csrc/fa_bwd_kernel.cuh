@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_ld64_wait(t_lane + kColS + 64u * half, sv);
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarSRead + 0));  // S columns free for S_{j+1}
+            if (elect_one_sync()) mbar_arrive(bar(L::kBarSRead + 0));  // S columns free for S_{j+1}
             // keys visible to this row in this tile: c <= last
             int last = p.N - 1 - j * 128;
             if (p.causal && j == qt) last = min(last, row);
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_ld64_wait(t_lane + kColDP + 64u * half, dv);
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarSRead + 1));  // dP columns free for dP_{j+1}
+            if (elect_one_sync()) mbar_arrive(bar(L::kBarSRead + 1));  // dP columns free for dP_{j+1}
             // dS buffer j & 1 last held dS(j-2): its dQ product must have read it
             if (j >= 2)
                 ok = fa_wait_warp(bar(L::kBarUsed + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort_flag, limit,
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarDSFull));
+            if (elect_one_sync()) mbar_arrive(bar(L::kBarDSFull));
         }
         if (ok && n_kv > 0) ok = fa_wait_warp(bar(L::kBarFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);
         if (ok) {
@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarDSFull + 0));
+            if (elect_one_sync()) mbar_arrive(bar(L::kBarDSFull + 0));
             // Phase 2, once dP^T is in: dS = P (dP - D), for the dK product
             ok = fa_wait_warp(bar(L::kBarSFull + 1), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
             if (!ok) break;
@@ -667,7 +667,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarDSFull + 1));
+            if (elect_one_sync()) mbar_arrive(bar(L::kBarDSFull + 1));
         }
         cp_async_wait_all();  // after an abort a prefetch may still be in flight
         if (ok && n_q > 0) ok = fa_wait_warp(bar(L::kBarFinal), 0, abort_flag, limit, kStatusSoftmaxWaitO);

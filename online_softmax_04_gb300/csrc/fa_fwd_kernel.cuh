@@ -786,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S_g is in registers: the buffer may take S_{g+2}
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::kBarSFree + b));
+                if (elect_one_sync()) mbar_arrive(bar(L::kBarSFree + b));
                 if constexpr (!kMask) {
                     // mask keys past the diagonal (causal) and past the end of the sequence
                     int lim = p.N - 1 - (w.j0 + j) * kBlockN;
@@ -840,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_new = move ? m_cand : m_prev;
                 xref[wg * kBlockM + row] = m_new;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::kBarXRef + quarter * 2 + wg));
+                if (elect_one_sync()) mbar_arrive(bar(L::kBarXRef + quarter * 2 + wg));
                 const bool any_move = __any_sync(0xffffffffu, move);
                 // bring this group's sums to the new reference (its last step may be
                 // two or more moves back)
@@ -895,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::kBarPFull + b));
+                if (elect_one_sync()) mbar_arrive(bar(L::kBarPFull + b));
             }
             if (!ok) break;
             // whole-row state: both groups' sums brought to the later (larger) reference.
@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 xs[(wg * 3 + 1) * kBlockM + row] = l_run;
                 xs[(wg * 3 + 2) * kBlockM + row] = l32_run;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::kBarXSum + quarter));
+                if (elect_one_sync()) mbar_arrive(bar(L::kBarXSum + quarter));
                 ok = fa_wait_warp(bar(L::kBarXSum + quarter), (uint32_t)(t & 1), abort_flag, limit,
                                   kStatusSoftmaxWaitX);
                 if (!ok) break;
@@ -950,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O has been read out of TMEM: the next tile's first P V may overwrite it
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::kBarOFree));
+                if (elect_one_sync()) mbar_arrive(bar(L::kBarOFree));
             } else {
                 // this thread's half row of O in one load; the next tile's first P V
                 // may overwrite O as soon as it is in registers
@@ -961,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32_wait(o_col, r);
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::kBarOFree));
+                if (elect_one_sync()) mbar_arrive(bar(L::kBarOFree));
                 // O/l -> bf16, straight from registers to the half row: 32-byte
                 // stores when O is 32-byte aligned (full L2 sectors), else 16-byte.
                 // (Staging through shared memory for coalesced or tensor stores
