@@ -400,9 +400,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// dK, dV: one CTA per (key tile, head).  TMEM: S^T [0,128) (P^T bf16 over its
-// columns [0,32) and [64,96)), dP^T [128,256) (dS^T bf16 likewise),
-// dV [256, 256+D), dK [256+D, 256+2D).
+// dK, dV: one CTA per (key tile, head).  TMEM: S^T [0,128), dP^T [128,256),
+// dV [256, 256+D), dK [256+D, 256+2D).  The bf16 operands P^T and dS^T:
+//  * D = 128 (TMEM full): over the columns they are formed from, [0,32) and
+//    [64,96) of S^T (resp. dP^T), so a score product waits until the gradient
+//    product of the step before has read them;
+//  * D = 64: in columns of their own, P^T [384,448), dS^T [448,512), so the
+//    next score product starts as soon as the compute warps hold the scores
+//    in registers, and only the operand store waits for the gradient product.
 // ---------------------------------------------------------------------------
 template <int D, int NS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -411,6 +416,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       const BwdParams p) {
     using L = BwdSmem<D, NS>;
     constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    constexpr bool kSepOp = 256 + 2 * D + 128 <= kTmemCols;  // operands in columns of their own
+    constexpr uint32_t kColOp0 = kSepOp ? 256 + 2 * D : kColS, kColOp1 = kSepOp ? 256 + 2 * D + 64 : kColDP;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -440,6 +447,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::kBarFinal), 2);
         mbar_init(bar(L::kBarDrain), 1);
         mbar_init(bar(L::kBarDrain + 1), 1);
+        mbar_init(bar(L::kBarSRead + 0), 8);  // S^T in registers (separate operand columns only)
+        mbar_init(bar(L::kBarSRead + 1), 8);  // dP^T in registers
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_q);
@@ -503,46 +512,102 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t col_acc = u == 0 ? kColDV : kColDK;
             const uint64_t ad = sdesc_sw128(res_a, 16, 1024);
             bool ok = fa_wait_warp(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
-            for (int i = 0; ok && i < n_q; ++i) {
-                const int s = i % NS;
-                const uint32_t b_sc = u == 0 ? ring_q(s) : ring_do(s);   // B of the score product
-                const uint32_t b_acc = u == 0 ? ring_do(s) : ring_q(s);  // B of the gradient product
-                ok = fa_wait_warp(bar(L::kBarFull + s), (uint32_t)((i / NS) & 1), abort_flag, limit,
-                                  kStatusMmaWaitK);
-                // this thread's score columns hold its bf16 operand of step i-1 until its
-                // gradient product has finished
-                if (ok && i > 0)
-                    ok = fa_wait_warp(bar(L::kBarUsed + u), (uint32_t)((i - 1) & 1), abort_flag, limit,
-                                      kStatusMmaWaitSFree);
-                if (!ok) break;
-                tc_fence_after_sync();
-                const uint64_t bd = sdesc_sw128(b_sc, 16, 1024);
-                if (elect_one_sync()) {
+            if constexpr (kSepOp) {
+                const uint32_t col_op = u == 0 ? kColOp0 : kColOp1;  // its bf16 operand
+                // the score product of step i, once Q_i / dO_i have landed and the compute
+                // warps hold the scores of step i-1 in registers
+                auto score = [&](int i) -> bool {
+                    const int s = i % NS;
+                    bool k = fa_wait_warp(bar(L::kBarFull + s), (uint32_t)((i / NS) & 1), abort_flag, limit,
+                                          kStatusMmaWaitK);
+                    if (k && i > 0)
+                        k = fa_wait_warp(bar(L::kBarSRead + u), (uint32_t)((i - 1) & 1), abort_flag, limit,
+                                         kStatusMmaWaitSFree);
+                    if (!k) return false;
+                    tc_fence_after_sync();
+                    const uint64_t bd = sdesc_sw128(u == 0 ? ring_q(s) : ring_do(s), 16, 1024);
+                    if (elect_one_sync()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u) >> 4;
-                        mma_ss(tmem + col_sc, sdesc_add_lo(ad, off), sdesc_add_lo(bd, off), kIdescS, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = ((uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                            mma_ss(tmem + col_sc, sdesc_add_lo(ad, off), sdesc_add_lo(bd, off), kIdescS, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::kBarSFull + u));
                     }
-                    tc_commit(bar(L::kBarSFull + u));
-                }
-                __syncwarp();
-                // its bf16 operand: P^T (written first) or dS^T
-                ok = fa_wait_warp(bar(L::kBarDSFull + u), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
-                if (!ok) break;
-                tc_fence_after_sync();
-                // the bf16 operands of queries 16 kk .. 16 kk + 15 sit at column
-                // 8 kk (first half of the queries) or 32 + 8 kk (second half); the B rows
-                // advance 2048 bytes per 16 queries
-                const uint64_t gd = sdesc_sw128(b_acc, kChunkBytes, 1024);
-                if (elect_one_sync()) {
+                    __syncwarp();
+                    return true;
+                };
+                // the gradient product of step i, once its bf16 operand (P^T, written
+                // first, or dS^T) is in TMEM
+                auto gradient = [&](int i) -> bool {
+                    const int s = i % NS;
+                    if (!fa_wait_warp(bar(L::kBarDSFull + u), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP))
+                        return false;
+                    tc_fence_after_sync();
+                    // the operands of queries 16 kk .. 16 kk + 15 sit at column 8 kk; the B rows
+                    // advance 2048 bytes per 16 queries
+                    const uint64_t gd = sdesc_sw128(u == 0 ? ring_do(s) : ring_q(s), kChunkBytes, 1024);
+                    if (elect_one_sync()) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + col_acc, tmem + col_sc + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
-                               sdesc_add_lo(gd, (uint32_t)kk * 128u), kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar(L::kBarEmpty + s));
-                    tc_commit(bar(L::kBarUsed + u));
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tmem + col_acc, tmem + col_op + (uint32_t)kk * 8u,
+                                   sdesc_add_lo(gd, (uint32_t)kk * 128u), kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+                        // covers every earlier product of this thread that read stage s
+                        tc_commit(bar(L::kBarEmpty + s));
+                        tc_commit(bar(L::kBarUsed + u));
+                    }
+                    __syncwarp();
+                    return true;
+                };
+                // the score product of step i+1 goes ahead of the gradient product of step i
+                if (ok && n_q > 0) ok = score(0);
+                for (int i = 0; ok && i < n_q; ++i) {
+                    if (i + 1 < n_q) ok = score(i + 1);
+                    ok = ok && gradient(i);
                 }
-                __syncwarp();
+            } else {
+                for (int i = 0; ok && i < n_q; ++i) {
+                    const int s = i % NS;
+                    const uint32_t b_sc = u == 0 ? ring_q(s) : ring_do(s);   // B of the score product
+                    const uint32_t b_acc = u == 0 ? ring_do(s) : ring_q(s);  // B of the gradient product
+                    ok = fa_wait_warp(bar(L::kBarFull + s), (uint32_t)((i / NS) & 1), abort_flag, limit,
+                                      kStatusMmaWaitK);
+                    // the score columns hold this thread's bf16 operand of step i-1 until its
+                    // gradient product has finished
+                    if (ok && i > 0)
+                        ok = fa_wait_warp(bar(L::kBarUsed + u), (uint32_t)((i - 1) & 1), abort_flag, limit,
+                                          kStatusMmaWaitSFree);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint64_t bd = sdesc_sw128(b_sc, 16, 1024);
+                    if (elect_one_sync()) {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = ((uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                            mma_ss(tmem + col_sc, sdesc_add_lo(ad, off), sdesc_add_lo(bd, off), kIdescS,
+                                   kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::kBarSFull + u));
+                    }
+                    __syncwarp();
+                    // its bf16 operand: P^T (written first) or dS^T
+                    ok = fa_wait_warp(bar(L::kBarDSFull + u), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    // the bf16 operands of queries 16 kk .. 16 kk + 15 sit at column 8 kk (first
+                    // half of the queries) or 32 + 8 kk (second half); the B rows advance 2048
+                    // bytes per 16 queries
+                    const uint64_t gd = sdesc_sw128(b_acc, kChunkBytes, 1024);
+                    if (elect_one_sync()) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ts(tmem + col_acc, tmem + col_sc + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
+                                   sdesc_add_lo(gd, (uint32_t)kk * 128u), kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bar(L::kBarEmpty + s));
+                        tc_commit(bar(L::kBarUsed + u));
+                    }
+                    __syncwarp();
+                }
             }
             if (elect_one_sync()) {
                 if (ok && n_q > 0) tc_commit(bar(L::kBarFinal));
@@ -597,12 +662,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const bool diag = p.causal && qi == kt;
             const int first = diag ? row : 0;
             const uint64_t c2x2 = f32x2_pack(c2, c2);
-            // P^T and dS^T of query columns [64 half, +64) go to columns [64 half,
-            // 64 half + 32): inside what this warp has already read (64 half + 16 hc +
-            // 16 <= 64 half + 32 hc + 32), never into the other half's columns.
+            // P^T and dS^T of query columns [64 half, +64) go to operand columns
+            // [32 half, 32 half + 32) of their own (separate operand columns), or over
+            // the scores to [64 half, 64 half + 32): inside what this warp has already
+            // read (64 half + 16 hc + 16 <= 64 half + 32 hc + 32), never into the other
+            // half's columns.
+            const uint32_t op_off = kSepOp ? 32u * (uint32_t)half : 64u * (uint32_t)half;
             // Phase 1, as soon as S^T is in: P, stored as bf16 for the dV product
             // (which starts at once) and kept in fp32 for dS.
             ok = fa_wait_warp(bar(L::kBarSFull + 0), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            // separate operand columns: P^T of step i-1 must have been read by its dV product
+            if (kSepOp && ok && i > 0)
+                ok = fa_wait_warp(bar(L::kBarUsed + 0), (uint32_t)((i - 1) & 1), abort_flag, limit,
+                                  kStatusSoftmaxWaitPV);
             if (!ok) break;
             tc_fence_after_sync();
             float pf[64];
@@ -611,6 +683,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int ch = 2 * half + hc;
                 uint32_t sv[32], pk[16];
                 tmem_ld32_wait(t_lane + kColS + 32u * ch, sv);
+                if (kSepOp && hc == 1) {  // S^T is in registers: its columns may take S^T(i+1)
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (elect_one_sync()) mbar_arrive(bar(L::kBarSRead + 0));
+                }
                 if (!diag) {
                     // packed fp32x2 arithmetic; -LSE of two queries per load
 #pragma unroll
@@ -636,7 +713,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
 #pragma unroll
                 for (int i2 = 0; i2 < 16; ++i2) pk[i2] = pack_bf16x2(pf[32 * hc + 2 * i2], pf[32 * hc + 2 * i2 + 1]);
-                tmem_st16(t_lane + kColS + 64u * half + 16u * hc, pk);
+                tmem_st16(t_lane + kColOp0 + op_off + 16u * hc, pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -644,6 +721,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (elect_one_sync()) mbar_arrive(bar(L::kBarDSFull + 0));
             // Phase 2, once dP^T is in: dS = P (dP - D), for the dK product
             ok = fa_wait_warp(bar(L::kBarSFull + 1), (uint32_t)(i & 1), abort_flag, limit, kStatusSoftmaxWaitS);
+            if (kSepOp && ok && i > 0)  // dS^T of step i-1 read by its dK product
+                ok = fa_wait_warp(bar(L::kBarUsed + 1), (uint32_t)((i - 1) & 1), abort_flag, limit,
+                                  kStatusSoftmaxWaitPV);
             if (!ok) break;
             tc_fence_after_sync();
 #pragma unroll
@@ -651,6 +731,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int ch = 2 * half + hc;
                 uint32_t dv[32], dk[16];
                 tmem_ld32_wait(t_lane + kColDP + 32u * ch, dv);
+                if (kSepOp && hc == 1) {  // dP^T is in registers: its columns may take dP^T(i+1)
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (elect_one_sync()) mbar_arrive(bar(L::kBarSRead + 1));
+                }
 #pragma unroll
                 for (int i2 = 0; i2 < 16; ++i2) {
                     const int c0 = 32 * ch + 2 * i2;
@@ -662,7 +747,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  d0, d1);
                     dk[i2] = pack_bf16x2(d0, d1);
                 }
-                tmem_st16(t_lane + kColDP + 64u * half + 16u * hc, dk);
+                tmem_st16(t_lane + kColOp1 + op_off + 16u * hc, dk);
             }
             tmem_st_wait();
             tc_fence_before_sync();

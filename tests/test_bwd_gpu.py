@@ -81,12 +81,15 @@ def test_backward_every_row(fa, B, H, N, d, causal):
     check(fa, B, H, N, d, causal, seed=N * 3 + d, label=f"B{B}H{H}N{N}d{d} causal={causal}")
 
 
-def test_backward_late_max_rows_sampled(fa):
-    """Large, growing scores (the late-max distribution) at N = 2048, sampled rows."""
-    B, H, N, d = 1, 4, 2048, 128
+@pytest.mark.parametrize("d,causal", [(128, True), (64, True), (64, False)])
+def test_backward_late_max_rows_sampled(fa, d, causal):
+    """Large, growing scores (the late-max distribution) at N = 2048, sampled rows: 16 query
+    steps per key tile (up to 16 per query tile), many turns of every barrier's phase."""
+    B, H, N = 1, 4, 2048
     rng = np.random.default_rng(5)
     rows = np.unique(np.concatenate([rng.integers(0, B * H * N, 200), [0, N - 1, B * H * N - 1]])).astype(np.int64)
-    check(fa, B, H, N, d, True, seed=77, q_rows=rows, k_rows=rows[::-1].copy(), label="late N2048", dist="late")
+    check(fa, B, H, N, d, causal, seed=77 + d, q_rows=rows, k_rows=rows[::-1].copy(),
+          label=f"late N2048 d{d} causal={causal}", dist="late")
 
 
 def test_zero_upstream_gradient_gives_zero(fa):
