@@ -155,7 +155,10 @@ def kernel_source_hash() -> str:
     for name in sorted(os.listdir(csrc)):
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(strip_c_comments(f.read()).encode())
+            # lines left blank by the comments are dropped, so adding or removing a
+            # comment line does not change the hash either
+            lines = (ln.rstrip() for ln in strip_c_comments(f.read()).splitlines())
+            h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -29,7 +29,10 @@
 //     and an S buffer are free, the other the P V products as soon as P_j is
 //     written.  A tcgen05.mma burst keeps its issuing thread busy until the
 //     tensor pipe has taken it, so two issuers keep the pipe fed while either
-//     one waits on a barrier.
+//     one waits on a barrier.  Every instruction an issuer runs between
+//     products costs feed rate, so the whole warp runs the loop (waits,
+//     counters, descriptors built once per product and advanced by a 32-bit
+//     add per K step) and an elect.sync lane issues the products and commits.
 //   * P_j is written back to TMEM as bf16 and consumed from there as the A
 //     operand of P V (no shared-memory round trip).
 //   * Q, K_j and V_j are brought in by TMA (128-byte swizzle) into rings of

@@ -88,3 +88,20 @@ def test_source_hash_ignores_comments():
     assert strip(code) == code
     assert strip(with_comments).split() == strip(code).split()
     assert strip("int x; /* unterminated") == "int x;  "
+
+
+def test_source_hash_ignores_comment_lines(tmp_path, monkeypatch):
+    """Adding whole comment lines (and the blank lines they leave) keeps the hash; a code
+    change does not."""
+    import bench
+
+    src = tmp_path / "online_softmax_04_gb300" / "csrc"
+    src.mkdir(parents=True)
+    f = src / "k.cuh"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f.write_text("int a = 1;\nint b = 2;\n")
+    h0 = bench.kernel_source_hash()
+    f.write_text("// header\n//   more\nint a = 1;  // one\n\n// note\nint b = 2;\n")
+    assert bench.kernel_source_hash() == h0
+    f.write_text("int a = 1;\nint b = 3;\n")
+    assert bench.kernel_source_hash() != h0
