@@ -204,7 +204,7 @@ int fa_splitkv_auto_splits(int B, int H, int N, int d, int causal);
  * unchanged ([B][H][N][d] bf16, lse [B][H][N] fp32), because the heads are
  * independent problems ("Online Softmax: Tiling Across a Reduction": each
  * query row's softmax needs only its own scores).  The call walks the B*H
- * heads in chunks of heads_per_chunk through two device slots in `workspace`,
+ * heads in chunks of heads_per_chunk through three device slots in `workspace`,
  * on three streams.  It copies chunk c+1 to the device, runs the forward kernel
  * on chunk c, and copies chunk c-1's o and lse back, all at once.
  *
@@ -229,7 +229,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
                 int causal, float scale, int heads_per_chunk, void* workspace, size_t workspace_bytes,
                 fa_stream_t stream);
 
-/* Device workspace fa_fwd_host needs (two slots of one chunk's q, k, v, o and lse); 0 for bad arguments. */
+/* Device workspace fa_fwd_host needs (three slots of one chunk's q, k, v, o and lse); 0 for bad arguments. */
 size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chunk);
 
 /*

@@ -309,9 +309,15 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
 }
 
 // ---------------------------------------------------------------------------
-// fa_fwd_host: host-resident tensors streamed through two device slots
+// fa_fwd_host: host-resident tensors streamed through three device slots
 // ---------------------------------------------------------------------------
 constexpr size_t kHostAlign = 256;
+// Chunk c's inputs wait for the read-back of the chunk that used its slot
+// before, c - kHostSlots.  With two slots that read-back (chunk c - 2: its
+// kernel and copy-out) ends after chunk c - 1's input copy, and the input
+// stream, which the host link limits, stalls on every chunk; with three it
+// ends long before.
+constexpr int kHostSlots = 3;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -332,7 +338,7 @@ struct HostPipe {
     bool ready = false;
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t start = nullptr, end = nullptr;
-    cudaEvent_t in_done[2] = {}, compute_done[2] = {}, out_done[2] = {};
+    cudaEvent_t in_done[kHostSlots] = {}, compute_done[kHostSlots] = {}, out_done[kHostSlots] = {};
 };
 HostPipe g_host_pipe[kMaxDevices];
 std::mutex g_host_mu;  // serialises the enqueue of fa_fwd_host calls (shared streams and events)
@@ -348,7 +354,7 @@ int host_pipe(HostPipe** out) {
                   cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaEventCreateWithFlags(&hp.start, ev) == cudaSuccess &&
                   cudaEventCreateWithFlags(&hp.end, ev) == cudaSuccess;
-        for (int i = 0; ok && i < 2; ++i)
+        for (int i = 0; ok && i < kHostSlots; ++i)
             ok = cudaEventCreateWithFlags(&hp.in_done[i], ev) == cudaSuccess &&
                  cudaEventCreateWithFlags(&hp.compute_done[i], ev) == cudaSuccess &&
                  cudaEventCreateWithFlags(&hp.out_done[i], ev) == cudaSuccess;
@@ -518,7 +524,7 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chu
     if ((d != 64 && d != 128) || B < 1 || H < 1 || N < 1) return 0;
     const long long BH = (long long)B * (long long)H;
     if (heads_per_chunk < 0 || heads_per_chunk > BH) return 0;
-    return 2 * host_slot_bytes(host_chunk_heads(BH, heads_per_chunk), N, d);
+    return kHostSlots * host_slot_bytes(host_chunk_heads(BH, heads_per_chunk), N, d);
 }
 
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -532,7 +538,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     if ((reinterpret_cast<uintptr_t>(workspace) & (kHostAlign - 1)) != 0) return FA_ERR_ALIGNMENT;
     const int hc = host_chunk_heads(BH, heads_per_chunk);
     const size_t slot = host_slot_bytes(hc, N, d);
-    if (workspace_bytes < 2 * slot) return FA_ERR_WORKSPACE;
+    if (workspace_bytes < kHostSlots * slot) return FA_ERR_WORKSPACE;
     rc = check_device();
     if (rc != FA_OK) return rc;
 
@@ -547,7 +553,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
               cudaStreamWaitEvent(hp->d2h, hp->start, 0) == cudaSuccess;
     const long long n_chunks = (BH + hc - 1) / hc;
     for (long long c = 0; ok && c < n_chunks; ++c) {
-        const int sl = (int)(c & 1);
+        const int sl = (int)(c % kHostSlots);
         const long long h0 = c * hc;
         const int nh = (int)std::min<long long>(hc, BH - h0);
         uint8_t* base = static_cast<uint8_t*>(workspace) + (size_t)sl * slot;
@@ -559,7 +565,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
         const size_t off = (size_t)h0 * head_elems * 2u;  // byte offset of the chunk's first head
         const size_t bytes = (size_t)nh * head_elems * 2u;
         // inputs: once the slot's previous chunk has been read back
-        if (c >= 2) ok = cudaStreamWaitEvent(hp->h2d, hp->out_done[sl], 0) == cudaSuccess;
+        if (c >= kHostSlots) ok = cudaStreamWaitEvent(hp->h2d, hp->out_done[sl], 0) == cudaSuccess;
         ok = ok && cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + off, bytes, cudaMemcpyDefault, hp->h2d) == cudaSuccess &&
              cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + off, bytes, cudaMemcpyDefault, hp->h2d) == cudaSuccess &&
              cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + off, bytes, cudaMemcpyDefault, hp->h2d) == cudaSuccess &&

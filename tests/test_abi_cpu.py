@@ -188,9 +188,9 @@ def test_host_streamed_validation(fa):
     ws = FAKE + (5 << 30)
     B, H, N, d = 2, 3, 200, 64
     need = fa.fa_fwd_host_workspace_bytes(B, H, N, d, 2)
-    # two slots of 2 heads: q, k, v, o (2*200*64*2 = 51200 B each, 256-aligned) and lse (1600 -> 1792 B)
-    assert need == 2 * (4 * 51200 + 1792)
-    assert fa.fa_fwd_host_workspace_bytes(B, H, N, d, 0) == 2 * (4 * 25600 + 1024)  # ceil(6 / 8) = 1 head
+    # three slots of 2 heads: q, k, v, o (2*200*64*2 = 51200 B each, 256-aligned) and lse (1600 -> 1792 B)
+    assert need == 3 * (4 * 51200 + 1792)
+    assert fa.fa_fwd_host_workspace_bytes(B, H, N, d, 0) == 3 * (4 * 25600 + 1024)  # ceil(6 / 8) = 1 head
     assert fa.fa_fwd_host_workspace_bytes(B, H, N, d, 7) == 0
     assert fa.fa_fwd_host_workspace_bytes(B, H, N, 96, 1) == 0
 

@@ -1,5 +1,5 @@
-"""fa_fwd_host: the forward on host-resident tensors, streamed through a device
-workspace in chunks of heads.  The per-tile arithmetic is the one fa_fwd
+"""fa_fwd_host: the forward on host-resident tensors, streamed through a three-slot
+device workspace in chunks of heads.  The per-tile arithmetic is the one fa_fwd
 runs, so the results must equal fa_fwd's bit for bit (fa_fwd itself is held to
 the fp64 oracle in test_fa_gpu.py); every chunking, ragged last chunk, pinned
 and pageable host memory, and back-to-back calls that reuse one workspace.
@@ -40,6 +40,7 @@ CASES = [  # (B, H, N, d, causal, heads_per_chunk, pinned)
     (2, 4, 384, 128, False, 3, False),   # pageable host memory; chunks 3, 3, 2
     (1, 2, 129, 64, False, 2, True),     # one chunk holds every head
     (1, 16, 2048, 128, True, 4, True),   # four chunks, several persistent rounds each
+    (1, 7, 513, 64, True, 1, True),      # seven chunks: every one of the three slots reused
 ]
 
 
