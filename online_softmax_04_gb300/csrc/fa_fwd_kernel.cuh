@@ -57,6 +57,10 @@
 //     rows; LSE uses the fp32 sum of the unrounded exponentials.  At d = 128
 //     the softmax threads add the rounded weights; at d = 64 the tensor core
 //     does, in extra columns of the P V product (see FaSmem::kTcSum).
+//   * The row maximum of a step comes with the S read-out: the TMEM load's max
+//     reduction over the 128 loaded columns.  Rows with masked keys in the
+//     tile (diagonal, sequence end, windows, documents) reduce the masked
+//     values instead.
 //   * Epilogue: each group reads its half of O's columns out of TMEM in one
 //     load, releases O to the next tile's first P V product at once, then
 //     normalises and stores its half rows.
@@ -780,12 +784,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 float s[kBlockN];
+                float ld_max;  // the maximum of the 128 loaded scores, from the load itself
                 {
                     uint32_t r[kBlockN];
-                    tmem_ld128_wait(t_lane + L::col_s(b), r);
+                    tmem_ld128_max_wait(t_lane + L::col_s(b), r, ld_max);
 #pragma unroll
                     for (int i = 0; i < kBlockN; ++i) s[i] = __uint_as_float(r[i]);
                 }
+                bool masked = false;  // some key of this row is masked in this tile
                 // S_g is in registers: the buffer may take S_{g+2}
                 tc_fence_before_sync();
                 __syncwarp();
@@ -795,6 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int lim = p.N - 1 - (w.j0 + j) * kBlockN;
                     if (p.causal && w.j0 + j == w.qt) lim = min(lim, row);
                     if (lim < kBlockN - 1) {
+                        masked = true;
 #pragma unroll
                         for (int i = 0; i < kBlockN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
                     }
@@ -806,22 +813,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int first = row_lo - k0;
                     const int last = min(row_hi, p.N - 1) - k0;
                     if (first > 0 || last < kBlockN - 1) {
-    #pragma unroll
+                        masked = true;
+#pragma unroll
                         for (int i = 0; i < kBlockN; ++i) s[i] = (i < first || i > last) ? -INFINITY : s[i];
                     }
                 }
-                float mx[4] = {fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), fmax3(s[6], s[7], s[8]),
-                               fmax3(s[9], s[10], s[11])};
+                // the row maximum: from the load, unless a key of the row is masked here
+                float row_max = ld_max;
+                if (__any_sync(0xffffffffu, masked)) {
+                    float mx[4] = {fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), fmax3(s[6], s[7], s[8]),
+                                   fmax3(s[9], s[10], s[11])};
 #pragma unroll
-                for (int i = 12; i + 8 <= kBlockN; i += 8) {
-                    mx[0] = fmax3(mx[0], s[i + 0], s[i + 1]);
-                    mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
-                    mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
-                    mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
+                    for (int i = 12; i + 8 <= kBlockN; i += 8) {
+                        mx[0] = fmax3(mx[0], s[i + 0], s[i + 1]);
+                        mx[1] = fmax3(mx[1], s[i + 2], s[i + 3]);
+                        mx[2] = fmax3(mx[2], s[i + 4], s[i + 5]);
+                        mx[3] = fmax3(mx[3], s[i + 6], s[i + 7]);
+                    }
+                    mx[0] = fmax3(mx[0], s[124], s[125]);
+                    mx[1] = fmax3(mx[1], s[126], s[127]);
+                    if (masked) row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 }
-                mx[0] = fmax3(mx[0], s[124], s[125]);
-                mx[1] = fmax3(mx[1], s[126], s[127]);
-                const float row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 // reference after step g-1, handed over by the other group (every step
                 // after the first waits, so the hand-overs stay in lock step; a new
                 // tile starts from -inf and ignores the value)
