@@ -205,8 +205,9 @@ int fa_splitkv_auto_splits(int B, int H, int N, int d, int causal);
  * independent problems ("Online Softmax: Tiling Across a Reduction": each
  * query row's softmax needs only its own scores).  The call walks the B*H
  * heads in chunks of heads_per_chunk through three device slots in `workspace`,
- * on three streams.  It copies chunk c+1 to the device, runs the forward kernel
- * on chunk c, and copies chunk c-1's o and lse back, all at once.
+ * on three streams.  While the forward kernel runs on chunk c, later chunks are
+ * copied to the device (chunk c+k waits only for the read-back of chunk
+ * c+k-3, whose slot it takes) and chunk c-1's o and lse are copied back.
  *
  *   heads_per_chunk  1 .. B*H, or 0 for ceil(B*H / 8)
  *   workspace        device memory, 256-byte aligned, at least
