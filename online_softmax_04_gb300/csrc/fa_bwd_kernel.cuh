@@ -23,15 +23,19 @@
 //     epilogue, so no atomics are needed.
 //   * fa_bwd_dkdv_sm103: one CTA per key tile (K, V resident; Q_i, dO_i
 //     streamed).  Per query tile: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM;
-//     the compute warps (thread = key row) write P^T and dS^T in bf16 over the
-//     columns they have just read; dV += P^T dO_i and dK += dS^T Q_i are TS
-//     products accumulating in TMEM.
+//     the compute warps (thread = key row) write P^T and dS^T in bf16 (over
+//     the columns they have just read at d = 128, into spare columns at
+//     d = 64); dV += P^T dO_i and dK += dS^T Q_i are TS products accumulating
+//     in TMEM.
 // Splitting dQ from dK/dV costs two extra products per tile pair (S and dP
 // are formed twice) and buys kernels with no cross-CTA reduction.
 //
-// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs, warps 4-11 compute: two warps per 32-row TMEM lane quarter,
-// each taking half of the 128 columns of a step and half of the epilogue.
+// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM, and
+// warps 1 and 3 issue the MMAs (dQ kernel: S and dP on warp 1, dQ on warp 3;
+// dK/dV kernel: S^T then dV on warp 1, dP^T then dK on warp 3), each running
+// its loop on the whole warp and issuing from an elect.sync lane.  Warps 4-11
+// compute: two warps per 32-row TMEM lane quarter, each taking half of the
+// 128 columns of a step and half of the epilogue.
 // Every barrier wait is bounded by the same watchdog as the forward kernel.
 #pragma once
 
