@@ -37,7 +37,19 @@
  * argument errors are detected on the host before anything is enqueued.
  * fa_strerror() names a code.  A kernel that waits longer than its
  * watchdog limit on an internal barrier abandons its tile, records a bit in
- * a device status word and exits; fa_get_device_status() reads that word.
+ * a device status word and exits; fa_get_last_error() and
+ * fa_get_device_status() read that word.  The forward kernels (fa_fwd,
+ * fa_fwd_masked, fa_fwd_splitkv, fa_fwd_splitkv_noalloc, fa_fwd_host) also
+ * write NaN into the lse of every row of the tile they abandon, so that an
+ * abort shows in the outputs; tiles a CTA had not started keep whatever the
+ * output buffers held, so the status word is the authoritative signal.
+ *
+ * Per-device state (the device addresses of the library's static arrays, and
+ * the internal streams and events of fa_fwd_host and fa_bwd) is set up by the
+ * first call on each device and kept for the life of the process.  After
+ * cudaDeviceReset() on a device, do not call this library on that device
+ * again in the same process: the cached addresses and handles belong to the
+ * destroyed context.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -307,6 +319,17 @@ const char* fa_strerror(int code);
  */
 int fa_get_device_status(unsigned int* status);
 
+/*
+ * fa_get_last_error -- the device-side timeout flag of the current device as
+ * an int: 0 when no kernel has given up on a barrier since the last
+ * fa_clear_device_status(), otherwise the (positive) status word of
+ * fa_get_device_status(), whose bits name the wait that ran out; FA_ERR_CUDA
+ * (negative) when the device could not be read.  It reports, it does not
+ * clear.  Synchronises with the device, so it is a debugging call, not one for
+ * the hot path.
+ */
+int fa_get_last_error(void);
+
 /* Reset the device status word of the current device to 0 (synchronous). */
 int fa_clear_device_status(void);
 
@@ -325,6 +348,20 @@ uint64_t fa_set_watchdog_ns(uint64_t ns);
  * *status.  Returns FA_OK or FA_ERR_CUDA.
  */
 int fa_watchdog_selftest(uint64_t ns, fa_stream_t stream, unsigned int* status);
+
+/*
+ * Watchdog self-test of the forward kernel itself: fa_fwd on one query tile
+ * (B = H = 1, 1 <= N <= 128) with its S products withheld, so that the softmax
+ * warps' first wait on S runs out after `ns` nanoseconds (at least 1e6).  The
+ * kernel then takes its abort path: it records the timeout bit, writes NaN into
+ * lse[0 .. N-1], leaves o untouched, lets its copies land, frees its tensor
+ * memory and returns; nothing faults or hangs.  Clears the status word first,
+ * synchronises `stream` and stores the word in *status.  Arguments as fa_fwd.
+ * Returns FA_OK, FA_ERR_SHAPE for N > 128, an fa_fwd argument error or
+ * FA_ERR_CUDA.
+ */
+int fa_watchdog_selftest_fwd(uint64_t ns, const void* q, const void* k, const void* v, void* o, float* lse, int N,
+                             int d, fa_stream_t stream, unsigned int* status);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int fa_version(void);

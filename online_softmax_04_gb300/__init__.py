@@ -87,6 +87,10 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd.restype = I
             L.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
             L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+            L.fa_get_last_error.argtypes = []
+            L.fa_get_last_error.restype = I
+            L.fa_watchdog_selftest_fwd.argtypes = [ctypes.c_uint64, P, P, P, P, P, I, I, P, ctypes.POINTER(ctypes.c_uint)]
+            L.fa_watchdog_selftest_fwd.restype = I
             L.fa_version.argtypes = []
             L.fa_version.restype = I
             _lib = L
@@ -344,6 +348,22 @@ def fa_set_watchdog_ns(ns: int) -> int:
 def fa_watchdog_selftest(ns: int, stream=None) -> int:
     st = ctypes.c_uint(0)
     rc = lib().fa_watchdog_selftest(int(ns), _stream(stream), ctypes.byref(st))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+    return st.value
+
+
+def fa_get_last_error() -> int:
+    """The device-side timeout flag: 0, the status word (> 0), or a negative FA code."""
+    return int(lib().fa_get_last_error())
+
+
+def fa_watchdog_selftest_fwd(ns: int, q, k, v, o, lse, N: int, d: int, stream=None) -> int:
+    """fa_fwd on one tile with its S products withheld: the watchdog must end the
+    softmax's wait; returns the device status word."""
+    st = ctypes.c_uint(0)
+    rc = lib().fa_watchdog_selftest_fwd(int(ns), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(N), int(d),
+                                        _stream(stream), ctypes.byref(st))
     if rc != FA_OK:
         raise FaError(rc, fa_strerror(rc))
     return st.value

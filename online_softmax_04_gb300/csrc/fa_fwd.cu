@@ -17,7 +17,7 @@
 
 namespace {
 
-constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kVersion = 1 * 10000 + 1 * 100 + 0;
 constexpr int kMaxDevices = 64;
 
 uint64_t g_watchdog_ns = 1000000000ull;  // 1 s
@@ -742,6 +742,32 @@ int fa_watchdog_selftest(uint64_t ns, fa_stream_t stream, unsigned int* status) 
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
     return fa_get_device_status(status);
+}
+
+int fa_watchdog_selftest_fwd(uint64_t ns, const void* q, const void* k, const void* v, void* o, float* lse, int N,
+                             int d, fa_stream_t stream, unsigned int* status) {
+    if (!status) return FA_ERR_NULL_POINTER;
+    if (N > fa::kBlockM) return FA_ERR_SHAPE;  // one query tile, so the one CTA starts every row
+    int rc = validate(q, k, v, o, lse, 1, 1, N, d, 1.0f);
+    if (rc != FA_OK) return rc;
+    Prepared pr;
+    rc = prepare(q, k, v, o, lse, 1, 1, N, d, 0, 1.0f / std::sqrt((float)d), &pr);
+    if (rc != FA_OK) return rc;
+    if (fa_clear_device_status() != FA_OK) return FA_ERR_CUDA;
+    pr.p.watchdog_ns = ns < 1000000ull ? 1000000ull : ns;
+    pr.p.withhold_s = 1;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rc = launch_d<false>(d, pr.tq, pr.tk, pr.tv, pr.p, pr.BH, s);
+    if (rc != FA_OK) return rc;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+    return fa_get_device_status(status);
+}
+
+int fa_get_last_error(void) {
+    unsigned int st = 0;
+    const int rc = fa_get_device_status(&st);
+    if (rc != FA_OK) return rc;
+    return (int)(st & 0x7fffffffu);
 }
 
 int fa_version(void) { return kVersion; }

@@ -132,6 +132,9 @@ struct FaParams {
     int causal;
     float scale_log2;  // scale * log2(e)
     unsigned long long watchdog_ns;
+    // watchdog self-test only: the S products are never issued, so the softmax
+    // warps' first wait runs out (0 in every real launch)
+    int withhold_s;
     // split-KV partial states (kSplit kernels only): [n_splits][B*H][N] rows
     int n_splits;
     float* ws_o;    // unnormalised O, fp32 [rows][d]
@@ -597,8 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok && j + 2 < w.n_kv) ok = load_k(w, j + 2);
                 }
             }
-            if (!ok || *abort_flag) {
-                // abort: let every copy already issued land before the CTA exits
+            {
+                // let every copy already issued land before the CTA exits: after an
+                // abort some are never consumed (in a normal run these waits succeed
+                // at once)
                 for (int qb = 0; qb < L::kQBufs; ++qb)
                     if (nq > qb)
                         fa_wait_drain(bar(L::kBarQ + qb), (uint32_t)(((nq - 1 - qb) / L::kQBufs) & 1), limit);
@@ -628,6 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t qa = sbase + L::kOffQ + (uint32_t)qb * L::kTileBytes;
                 ok = fa_wait_warp(bar(L::kBarQ + qb), (uint32_t)((t / L::kQBufs) & 1), abort_flag, limit,
                                   kStatusMmaWaitQ);
+                if (p.withhold_s) break;
                 for (int j = 0; ok && j < w.n_kv; ++j, ++g) {
                     const int b = g & 1;
                     const int ks = g % NK;
@@ -735,11 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c2 = p.scale_log2;
         int g = 0, t = 0;  // steps and non-empty tiles so far
         bool ok = true;
+        bool in_tile = false;  // a tile has been started and its rows not yet written
+        int q_idx = 0;
+        bool valid = false;
         Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
         TileWork w;
         while (ok && seq.template next<true>(p, w)) {
-            const int q_idx = w.qt * kBlockM + row;
-            const bool valid = q_idx < p.N;
+            q_idx = w.qt * kBlockM + row;
+            valid = q_idx < p.N;
             if constexpr (kSplit) {
                 if (w.n_kv == 0) {
                     // no key of this split is visible: an empty partial state
@@ -771,6 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     row_hi = min(row_hi, doc_last(dseq, q_idx, p.N));
                 }
             }
+            in_tile = true;
             float m_own = -INFINITY;  // reference this group's sums are relative to (base-2 units)
             float l_run = 0.f;        // this group's sum of bf16(2^(t - m_own)): normalises O
             float l32_run = 0.f;      // this group's fp32 sum of 2^(t - m_own): gives LSE
@@ -1003,7 +1013,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.lse[(size_t)w.bh * (size_t)p.N + (size_t)q_idx] =
                         l32_fin > 0.f ? (m_fin + lg2_approx(l32_fin)) * kLn2 : -INFINITY;
             }
+            in_tile = false;
             ++t;
+        }
+        if (!ok && in_tile && valid) {
+            // the watchdog ended a wait inside this tile: its rows are never
+            // finished, so their statistic is set to NaN (split-KV: the partial
+            // maximum, which the merge turns into a NaN LSE and O)
+            const float nan = __int_as_float(0x7fffffff);
+            if constexpr (kSplit)
+                p.ws_m[((size_t)blockIdx.z * gridDim.y + (size_t)w.bh) * (size_t)p.N + (size_t)q_idx] = nan;
+            else
+                p.lse[(size_t)w.bh * (size_t)p.N + (size_t)q_idx] = nan;
         }
         __syncwarp();
     }

@@ -25,8 +25,8 @@ def declared_functions(path):
 
 def test_exports_every_declared_symbol(fa):
     names = declared_functions(fa.HEADER_PATH)
-    assert {"fa_fwd", "fa_strerror", "fa_get_device_status", "fa_clear_device_status", "fa_set_watchdog_ns",
-            "fa_watchdog_selftest", "fa_version"} <= set(names)
+    assert {"fa_fwd", "fa_strerror", "fa_get_last_error", "fa_get_device_status", "fa_clear_device_status",
+            "fa_set_watchdog_ns", "fa_watchdog_selftest", "fa_watchdog_selftest_fwd", "fa_version"} <= set(names)
     raw = ctypes.CDLL(fa.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n

@@ -271,3 +271,29 @@ def test_watchdog_ends_a_wait_nothing_completes(fa):
     q, k, v = wl.make_inputs(w)
     o, lse = run_gpu(fa, q, k, v, True, w.scale)
     compare(o, lse, q, k, v, True, w.scale, all_rows(1, 1, 256), "after watchdog")
+    # the device-side timeout flag as the boundary's int: set by the self-test, 0 once cleared
+    assert fa.fa_watchdog_selftest(20_000_000) & (1 << 8)
+    assert fa.fa_get_last_error() & (1 << 8)
+    fa.fa_clear_device_status()
+    assert fa.fa_get_last_error() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_watchdog_abort_leaves_nan_lse(fa, d):
+    """The forward kernel's own abort path: its S products withheld, the softmax
+    warps' first wait runs out; the tile's lse rows read NaN, o is not written,
+    and the context stays usable."""
+    N = 100
+    w = wl.Workload("abort", 1, 1, N, d, False, "iid", 31)
+    q, k, v = (t.cuda() for t in wl.make_inputs(w))
+    o = torch.full_like(q, 3.0)
+    lse = torch.full((1, 1, N), 7.0, dtype=torch.float32, device="cuda")
+    st = fa.fa_watchdog_selftest_fwd(5_000_000, q, k, v, o, lse, N, d)
+    # the first wait to run out names itself: the softmax's wait on S, or the P V issuer's wait on P
+    assert st & ((1 << 5) | (1 << 3)), f"status {st:#x}"
+    assert torch.isnan(lse).all()
+    assert (o == 3.0).all()
+    fa.fa_clear_device_status()
+    assert fa.fa_get_last_error() == 0
+    o2, lse2 = run_gpu(fa, q.cpu(), k.cpu(), v.cpu(), False, w.scale)
+    compare(o2, lse2, q.cpu(), k.cpu(), v.cpu(), False, w.scale, all_rows(1, 1, N), "after abort")
