@@ -78,6 +78,24 @@ def oracle_rows(w, q, k, v, rows, return_threads: bool = False):
     return oracle.attention_three_pass(q, k, v, w.causal, w.scale, rows=rows, return_threads=return_threads)
 
 
+def l2_policy(w) -> tuple[bool, str]:
+    """Whether timed steps flush L2 first (inputs smaller than ~L2), and the sentence saying so."""
+    in_bytes = 3 * w.B * w.H * w.N * w.d * 2
+    if in_bytes < 1.25 * L2_BYTES:
+        return True, "L2 flushed (512 MB write, then 256 MB read) before each individually timed step"
+    return False, (f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB of Q, K, V > 129 MB), "
+                   "back-to-back steps, no flush")
+
+
+def bench_config(w, world: int) -> dict:
+    """The workload part of the JSON line, shared by both arms so that their configs compare equal."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "scale": "1/sqrt(d)", "flops_per_step_per_gpu": workload_flops(w), "l2": l2_policy(w)[1],
+            "parallelism": f"independent problem per GPU x{world}",
+            **({"window_left": w.window_left, "window_right": w.window_right, "doc_mean": w.doc_mean,
+                "flops": "4 d per visible (query, key) pair"} if w.masked else {})}
+
+
 def rank_workload(w, rank: int):
     """Every rank solves its own problem: the same shapes, its own seed."""
     return w.with_(seed=w.seed + 1000 * rank)
@@ -577,7 +595,8 @@ def run_reference(args, w, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "config": bench_config(w, world),
+        "entry_point": "oracle.attention_three_pass (fp64, host cores)",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": int(used), "kind": "oracle",
                          "sample": f"{n} random query rows per step of {w.name}, fp64 three-pass route"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -683,9 +702,7 @@ def main():
 
     # Inputs (Q, K, V) well above L2 make back-to-back steps honest; smaller
     # workloads get L2 flushed (a 512 MB write, then a 256 MB read) before each individually timed step.
-    in_bytes = 3 * q.numel() * q.element_size()
-    io_bytes = 4 * q.numel() * q.element_size() + lse.numel() * lse.element_size()
-    flush_l2 = in_bytes < 1.25 * L2_BYTES
+    flush_l2 = l2_policy(w)[0]
     flusher = L2Flush(torch, dev) if flush_l2 else None
 
     per_step = []  # this rank's device time of each timed step (ms)
@@ -780,16 +797,9 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-                       "scale": "1/sqrt(d)", "flops_per_step_per_gpu": flops,
-                       "l2": ("L2 flushed (512 MB write, then 256 MB read) before each individually timed step" if flush_l2 else
-                              f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB of Q, K, V > 129 MB), "
-                              "back-to-back steps, no flush"),
-                       "parallelism": f"independent problem per GPU x{world}",
-                       "entry_point": ("fa_fwd_masked" if w.masked else "fa_fwd") if n_splits < 0
-                       else f"fa_fwd_splitkv (n_splits={n_splits})",
-                       **({"window_left": w.window_left, "window_right": w.window_right, "doc_mean": w.doc_mean,
-                           "flops": "4 d per visible (query, key) pair"} if w.masked else {})},
+            "config": bench_config(w, world),
+            "entry_point": ("fa_fwd_masked" if w.masked else "fa_fwd") if n_splits < 0
+            else f"fa_fwd_splitkv (n_splits={n_splits})",
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
