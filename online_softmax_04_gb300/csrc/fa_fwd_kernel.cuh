@@ -52,11 +52,16 @@
 //     reference is kept, exponentials up to 2^64 are accumulated in fp32 and
 //     the O rescale on TMEM is skipped.  exp(x - m) / sum exp(x - m) does not
 //     depend on m, so the result is unchanged.
-//   * O is divided by the sum of the bf16-rounded exponentials, the very
-//     weights the P V product uses, so O / l is a convex combination of V
-//     rows; LSE uses the fp32 sum of the unrounded exponentials.  At d = 128
-//     the softmax threads add the rounded weights; at d = 64 the tensor core
-//     does, in extra columns of the P V product (see FaSmem::kTcSum).
+//   * The P V product uses bf16-rounded weights.  O is divided by a sum that
+//     accounts for that rounding where it matters most, the largest weight,
+//     while LSE uses the fp32 sum of the unrounded exponentials.  At d = 64
+//     the tensor core forms the exact sum of the rounded weights in extra
+//     columns of the P V product (see FaSmem::kTcSum).  At d = 128 TMEM has
+//     no room for them; there the sum is the fp32 sum plus, for every key
+//     tile, bf16(p_max) - p_max of the tile's largest weight, recomputed from
+//     the row maximum.  When one key dominates a row, that is the exact sum
+//     of the rounded weights, and O / l returns that key's V row; elsewhere
+//     the roundings of the many comparable weights average out.
 //   * The row maximum of a step comes with the S read-out: the TMEM load's max
 //     reduction over the 128 loaded columns.  Rows with masked keys in the
 //     tile (diagonal, sequence end, windows, documents) reduce the masked
@@ -139,7 +144,7 @@ struct FaParams {
     int n_splits;
     float* ws_o;    // unnormalised O, fp32 [rows][d]
     float* ws_m;    // reference max, base-2 units
-    float* ws_lbf;  // sum of the bf16-rounded exponentials
+    float* ws_lbf;  // the sum that normalises O (rounded weights at d = 64; fp32 sum + max corrections at d = 128)
     float* ws_l32;  // fp32 sum of the exponentials
 };
 
@@ -243,12 +248,11 @@ __device__ __forceinline__ bool fa_wait_drain(uint32_t bar, uint32_t parity, uin
 }
 
 // Exponentials of NE keys of a row against the reference -neg_m (base 2):
-// P packed to bf16 pairs, the sum of the bf16-rounded values and the fp32 sum.
-template <int NE, bool kBfSum = true>
+// P packed to bf16 pairs, and the fp32 sum of the unrounded values.
+template <int NE>
 __device__ __forceinline__ void exp_row_tile(const float (&s)[NE], float c2, float neg_m, uint32_t (&pk)[NE / 2],
-                                             float& sum_bf, float& sum_f32) {
+                                             float& sum_f32) {
     const uint64_t c2x2 = f32x2_pack(c2, c2), negm2 = f32x2_pack(neg_m, neg_m);
-    float rs[4] = {0.f, 0.f, 0.f, 0.f};
     uint64_t r32[2] = {0ull, 0ull};  // packed (even, odd) fp32 partial sums
 #pragma unroll
     for (int i = 0; i < NE / 2; ++i) {
@@ -257,13 +261,11 @@ __device__ __forceinline__ void exp_row_tile(const float (&s)[NE], float c2, flo
         const float p0 = ex2_approx(x0);
         const float p1 = ex2_approx(x1);
         pk[i] = pack_bf16x2(p0, p1);
-        if constexpr (kBfSum) rs[i & 3] = add_bf16x2_f32(rs[i & 3], pk[i]);
         r32[i & 1] = fadd2(r32[i & 1], f32x2_pack(p0, p1));
     }
     float e0, e1, o0, o1;
     f32x2_unpack(r32[0], e0, o0);
     f32x2_unpack(r32[1], e1, o1);
-    sum_bf = (rs[0] + rs[1]) + (rs[2] + rs[3]);
     sum_f32 = (e0 + o0) + (e1 + o1);
 }
 
@@ -782,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             in_tile = true;
             float m_own = -INFINITY;  // reference this group's sums are relative to (base-2 units)
-            float l_run = 0.f;        // this group's sum of bf16(2^(t - m_own)): normalises O
+            float l_run = 0.f;        // this group's sum that normalises O (d = 128; d = 64 reads TMEM)
             float l32_run = 0.f;      // this group's fp32 sum of 2^(t - m_own): gives LSE
             for (int j = 0; j < w.n_kv; ++j, ++g) {
                 if ((g & 1) != wg) continue;
@@ -874,10 +876,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // a row with nothing visible yet keeps m = -inf and uses 0, so that its
                 // -inf scores give 0 rather than NaN
                 uint32_t pk[kBlockN / 2];
-                float sum_bf, sum_f32;
-                // with the sums on the tensor core (d = 64) only the fp32 sum is kept here
-                exp_row_tile<kBlockN, !L::kTcSum>(s, c2, (m_new == -INFINITY) ? 0.f : -m_new, pk, sum_bf, sum_f32);
-                l_run = l_run * a_l + sum_bf;
+                float sum_f32;
+                const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+                exp_row_tile<kBlockN>(s, c2, neg_m, pk, sum_f32);
+                if constexpr (!L::kTcSum) {
+                    // the sum that normalises O: the fp32 sum plus the bf16 rounding of
+                    // this tile's largest weight, recomputed from the row maximum with
+                    // the very operations the loop applied to it (fma, ex2, RN to bf16)
+                    const float p_max = ex2_approx(fmaf(row_max, c2, neg_m));
+                    const float r_max = __bfloat162float(__float2bfloat16_rn(p_max)) - p_max;
+                    l_run = l_run * a_l + (sum_f32 + r_max);
+                }
                 l32_run = l32_run * a_l + sum_f32;
                 if (g >= 2) {
                     // P buffer b last fed P_{g-2} V_{g-2}: that product must have read it

@@ -355,15 +355,5 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// acc + lo + hi of a packed bf16x2 word, with mixed-precision adds (exact widening)
-__device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t pk) {
-    asm("{\n\t.reg .b16 lo, hi;\n\t"
-        "mov.b32 {lo, hi}, %1;\n\t"
-        "add.rn.f32.bf16 %0, lo, %0;\n\t"
-        "add.rn.f32.bf16 %0, hi, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(pk));
-    return acc;
-}
 
 }  // namespace fa
