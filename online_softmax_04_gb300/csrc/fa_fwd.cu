@@ -93,18 +93,24 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
         // blockIdx.x runs from the last (longest causal) tile down: heaviest first
         grid = dim3((unsigned)p.n_tiles, (unsigned)BH, (unsigned)p.n_splits);
     } else {
-        // every persistent launch takes its own work counter (the dynamic tail)
-        const int qrc = queue_slot(&p.queue);
-        if (qrc != FA_OK) return qrc;
         const int sms = sm_count() > 0 ? sm_count() : 148;
         const long long pairs = fa::persistent_pairs(p);
         const long long tiles = (long long)BH * p.n_tiles;
-        const long long ctas = tiles < sms ? tiles : sms;
-        grid = dim3((unsigned)ctas, 1, 1);
-        // every full round of pairs is dealt out statically; the partial last
-        // round goes to the dynamic tail as single tiles, long ones first
-        // (measured best against 70-95% static)
-        p.static_rounds = (int)(pairs / ctas);
+        if (tiles <= sms) {
+            // one CTA per tile, each CTA's tile fixed by its index: no work counter
+            grid = dim3((unsigned)tiles, 1, 1);
+            p.static_rounds = -1;
+            p.queue = nullptr;
+        } else {
+            // every persistent launch takes its own work counter (the dynamic tail)
+            const int qrc = queue_slot(&p.queue);
+            if (qrc != FA_OK) return qrc;
+            grid = dim3((unsigned)sms, 1, 1);
+            // every full round of pairs is dealt out statically; the partial last
+            // round goes to the dynamic tail as single tiles, long ones first
+            // (measured best against 70-95% static)
+            p.static_rounds = (int)(pairs / sms);
+        }
     }
     kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;

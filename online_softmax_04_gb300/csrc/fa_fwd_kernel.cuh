@@ -130,7 +130,9 @@ struct FaParams {
     // doc[b][i]; -1 leaves a side unbounded.  Causal attention: window_right = 0.
     int window_left, window_right;
     const int* doc;       // int32 [B][N] document ids, non-decreasing along each sequence, or nullptr
-    int static_rounds;    // persistent schedule: rounds of tile pairs assigned statically per CTA
+    // persistent schedule: rounds of tile pairs assigned statically per CTA, or -1
+    // when the grid has one CTA per tile (CTA x takes tile x; no work counter)
+    int static_rounds;
     unsigned int* queue;  // persistent schedule: {next dynamic item, CTAs finished}, zero on entry, reset on exit
     int N;
     int n_tiles;       // ceil(N / 128) query (= key) tiles
@@ -385,6 +387,13 @@ struct TileSeq {
     // producer (one thread): choose the next tile and post it
     int round = 0, sub = 0;  // static phase: pair round and tile within the pair
     __device__ bool choose(const FaParams& p, int& bh, int& qt) {
+        if (p.static_rounds < 0) {
+            // one CTA per tile: no pairing or counter needed
+            if (round++ > 0) return false;
+            bh = (int)(blockIdx.x / (unsigned)p.n_tiles);
+            qt = p.n_tiles - 1 - (int)(blockIdx.x % (unsigned)p.n_tiles);
+            return true;
+        }
         while (round < p.static_rounds) {
             int ql, qs;
             pair_tiles(p, (long long)blockIdx.x + (long long)round * gridDim.x, bh, ql, qs);
@@ -1046,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if constexpr (kPersistent) {
         // the last CTA out leaves the counter at zero for the next launch
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0 && p.queue) {
             __threadfence();
             if (atomicAdd(p.queue + 1, 1u) == gridDim.x - 1) {
                 atomicExch(p.queue + 0, 0u);
