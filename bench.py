@@ -789,7 +789,11 @@ def main():
         achieved = flops / (ms_step * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": recorded_traffic(w.name) if n_splits < 0 else None,
-                    "peak_source": peak_src, "kernel": KERNEL_NAME if n_splits < 0 else KERNEL_NAME + " + merge"}
+                    "peak_source": peak_src, "kernel": KERNEL_NAME if n_splits < 0 else KERNEL_NAME + " + merge",
+                    # registers, shared memory, CTAs per SM and TMEM columns, from the runtime
+                    "resources": fa.fa_kernel_resources(
+                        w.d, fa.FA_KERNEL_FWD_MASKED if w.masked else
+                        (fa.FA_KERNEL_FWD_SPLITKV if n_splits > 0 else fa.FA_KERNEL_FWD))}
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, q, k, v)

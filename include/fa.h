@@ -363,6 +363,39 @@ int fa_watchdog_selftest(uint64_t ns, fa_stream_t stream, unsigned int* status);
 int fa_watchdog_selftest_fwd(uint64_t ns, const void* q, const void* k, const void* v, void* o, float* lse, int N,
                              int d, fa_stream_t stream, unsigned int* status);
 
+/*
+ * fa_kernel_resources -- what the runtime reports for one of the library's
+ * kernels at head dimension d (64 or 128), as launched: registers per thread,
+ * threads per CTA, dynamic and static shared memory, local memory per thread,
+ * resident CTAs per SM (cudaOccupancyMaxActiveBlocksPerMultiprocessor) and the
+ * tensor-memory columns it allocates.  A resource report, not part of the
+ * computation (the pages' "LLM kernels 3: attention and online softmax"
+ * reports the same figures for its kernels).
+ *
+ *   kernel : FA_KERNEL_FWD (fa_fwd, fa_fwd_host), FA_KERNEL_FWD_MASKED,
+ *            FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ, FA_KERNEL_BWD_DKDV.
+ *
+ * Returns FA_OK, FA_ERR_NULL_POINTER, FA_ERR_HEAD_DIM, FA_ERR_SHAPE for an
+ * unknown kernel, FA_ERR_DEVICE or FA_ERR_CUDA.
+ */
+enum {
+    FA_KERNEL_FWD = 0,
+    FA_KERNEL_FWD_MASKED = 1,
+    FA_KERNEL_FWD_SPLITKV = 2,
+    FA_KERNEL_BWD_DQ = 3,
+    FA_KERNEL_BWD_DKDV = 4
+};
+typedef struct {
+    int registers_per_thread;
+    int threads_per_cta;
+    int dynamic_smem_bytes;
+    int static_smem_bytes;
+    int local_bytes_per_thread;
+    int ctas_per_sm;
+    int tmem_columns;
+} fa_kernel_resources_t;
+int fa_kernel_resources(int d, int kernel, fa_kernel_resources_t* out);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int fa_version(void);
 

@@ -34,6 +34,13 @@ FA_ERR_WORKSPACE = -11
 FA_ERR_SCRATCH_LIMIT = -12
 FA_ERR_MASK = -13
 FA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+FA_KERNEL_FWD, FA_KERNEL_FWD_MASKED, FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ, FA_KERNEL_BWD_DKDV = range(5)
+
+
+class KernelResources(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("registers_per_thread", "threads_per_cta", "dynamic_smem_bytes",
+                                            "static_smem_bytes", "local_bytes_per_thread", "ctas_per_sm",
+                                            "tmem_columns")]
 
 _lock = threading.Lock()
 _lib = None
@@ -91,6 +98,8 @@ def lib() -> ctypes.CDLL:
             L.fa_get_last_error.restype = I
             L.fa_watchdog_selftest_fwd.argtypes = [ctypes.c_uint64, P, P, P, P, P, I, I, P, ctypes.POINTER(ctypes.c_uint)]
             L.fa_watchdog_selftest_fwd.restype = I
+            L.fa_kernel_resources.argtypes = [I, I, ctypes.POINTER(KernelResources)]
+            L.fa_kernel_resources.restype = I
             L.fa_version.argtypes = []
             L.fa_version.restype = I
             _lib = L
@@ -367,6 +376,15 @@ def fa_watchdog_selftest_fwd(ns: int, q, k, v, o, lse, N: int, d: int, stream=No
     if rc != FA_OK:
         raise FaError(rc, fa_strerror(rc))
     return st.value
+
+
+def fa_kernel_resources(d: int, kernel: int = FA_KERNEL_FWD) -> dict:
+    """Registers, shared memory, CTAs per SM and TMEM columns of one kernel, as the runtime reports them."""
+    r = KernelResources()
+    rc = lib().fa_kernel_resources(int(d), int(kernel), ctypes.byref(r))
+    if rc != FA_OK:
+        raise FaError(rc, fa_strerror(rc))
+    return {name: getattr(r, name) for name, _ in KernelResources._fields_}
 
 
 def fa_version() -> int:

@@ -371,6 +371,49 @@ int host_pipe(HostPipe** out) {
     return FA_OK;
 }
 
+// Resources of one kernel as the runtime reports them, with the dynamic shared
+// memory it is launched with.
+template <typename K>
+int kernel_resources(K kern, int threads, size_t dyn_smem, int tmem_cols, fa_kernel_resources_t* out) {
+    cudaFuncAttributes a{};
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, kern) != cudaSuccess)
+        return FA_ERR_CUDA;
+    int ctas = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, kern, threads, dyn_smem) != cudaSuccess) return FA_ERR_CUDA;
+    out->registers_per_thread = a.numRegs;
+    out->threads_per_cta = threads;
+    out->dynamic_smem_bytes = (int)dyn_smem;
+    out->static_smem_bytes = (int)a.sharedSizeBytes;
+    out->local_bytes_per_thread = (int)a.localSizeBytes;
+    out->ctas_per_sm = ctas;
+    out->tmem_columns = tmem_cols;
+    return FA_OK;
+}
+
+template <int D, int NK, int NV>
+int fwd_resources(int kernel, fa_kernel_resources_t* out) {
+    using L = fa::FaSmem<D, NK, NV>;
+    switch (kernel) {
+        case FA_KERNEL_FWD:
+            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, false, true, false>, fa::kThreads, L::kAlloc,
+                                    (int)fa::kTmemCols, out);
+        case FA_KERNEL_FWD_MASKED:
+            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, false, true, true>, fa::kThreads, L::kAlloc,
+                                    (int)fa::kTmemCols, out);
+        case FA_KERNEL_FWD_SPLITKV:
+            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, true, false, false>, fa::kThreads, L::kAlloc,
+                                    (int)fa::kTmemCols, out);
+        case FA_KERNEL_BWD_DQ:
+            return kernel_resources(fa::fa_bwd_dq_sm103<D, D == 64 ? 4 : 2>, fa::kBwdThreads,
+                                    fa::BwdSmem<D, D == 64 ? 4 : 2>::kAlloc, (int)fa::kTmemCols, out);
+        case FA_KERNEL_BWD_DKDV:
+            return kernel_resources(fa::fa_bwd_dkdv_sm103<D, D == 64 ? 4 : 2>, fa::kBwdThreads,
+                                    fa::BwdSmem<D, D == 64 ? 4 : 2>::kAlloc, (int)fa::kTmemCols, out);
+        default: return FA_ERR_SHAPE;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -774,6 +817,14 @@ int fa_get_last_error(void) {
     const int rc = fa_get_device_status(&st);
     if (rc != FA_OK) return rc;
     return (int)(st & 0x7fffffffu);
+}
+
+int fa_kernel_resources(int d, int kernel, fa_kernel_resources_t* out) {
+    if (!out) return FA_ERR_NULL_POINTER;
+    if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
+    const int dev_rc = check_device();
+    if (dev_rc != FA_OK) return dev_rc;
+    return d == 64 ? fwd_resources<64, 6, 6>(kernel, out) : fwd_resources<128, 2, 3>(kernel, out);
 }
 
 int fa_version(void) { return kVersion; }

@@ -26,7 +26,8 @@ def declared_functions(path):
 def test_exports_every_declared_symbol(fa):
     names = declared_functions(fa.HEADER_PATH)
     assert {"fa_fwd", "fa_strerror", "fa_get_last_error", "fa_get_device_status", "fa_clear_device_status",
-            "fa_set_watchdog_ns", "fa_watchdog_selftest", "fa_watchdog_selftest_fwd", "fa_version"} <= set(names)
+            "fa_set_watchdog_ns", "fa_watchdog_selftest", "fa_watchdog_selftest_fwd", "fa_kernel_resources",
+            "fa_version"} <= set(names)
     raw = ctypes.CDLL(fa.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
@@ -207,3 +208,12 @@ def test_host_streamed_validation(fa):
     assert call(w=ws + 128) == fa.FA_ERR_ALIGNMENT
     assert call(wb=need - 1) == fa.FA_ERR_WORKSPACE
     assert call(o=q + 64) == fa.FA_ERR_ALIAS
+
+
+def test_kernel_resources_host_checks(fa):
+    L = fa.lib()
+    r = fa.KernelResources()
+    assert L.fa_kernel_resources(64, 0, None) == fa.FA_ERR_NULL_POINTER
+    assert L.fa_kernel_resources(96, 0, ctypes.byref(r)) == fa.FA_ERR_HEAD_DIM
+    if not torch.cuda.is_available():
+        assert L.fa_kernel_resources(64, 0, ctypes.byref(r)) in (fa.FA_ERR_CUDA, fa.FA_ERR_DEVICE)

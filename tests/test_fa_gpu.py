@@ -297,3 +297,33 @@ def test_watchdog_abort_leaves_nan_lse(fa, d):
     assert fa.fa_get_last_error() == 0
     o2, lse2 = run_gpu(fa, q.cpu(), k.cpu(), v.cpu(), False, w.scale)
     compare(o2, lse2, q.cpu(), k.cpu(), v.cpu(), False, w.scale, all_rows(1, 1, N), "after abort")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_kernel_resources_report(fa, d):
+    """The runtime's view of the kernels as launched: one CTA per SM, the whole
+    tensor memory, no local memory (no spills), 384 threads."""
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sm >= 1
+    for kernel in (fa.FA_KERNEL_FWD, fa.FA_KERNEL_FWD_MASKED, fa.FA_KERNEL_FWD_SPLITKV, fa.FA_KERNEL_BWD_DQ,
+                   fa.FA_KERNEL_BWD_DKDV):
+        r = fa.fa_kernel_resources(d, kernel)
+        assert r["threads_per_cta"] == 384, r
+        assert r["ctas_per_sm"] == 1, r
+        assert r["tmem_columns"] == 512, r
+        assert 0 < r["registers_per_thread"] <= 168, r
+        assert r["local_bytes_per_thread"] == 0, r
+        assert 150 * 1024 < r["dynamic_smem_bytes"] <= 227 * 1024, r
+
+
+@pytest.mark.parametrize("heads,d,causal", [(None, 64, False), ("sm+1", 64, False), (None, 128, True)])
+def test_one_tile_per_cta_boundary(fa, heads, d, causal):
+    """N = 128, so each head is one query tile: as many heads as SMs gives each CTA
+    its tile by index; one more head takes the persistent schedule with its work
+    counter.  Every row against the oracle."""
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    H = sm + 1 if heads == "sm+1" else sm
+    w = wl.Workload(f"tiles-{H}", 1, H, 128, d, causal, "iid", 61 + H)
+    q, k, v = wl.make_inputs(w)
+    o, lse = run_gpu(fa, q, k, v, causal, w.scale)
+    compare(o, lse, q, k, v, causal, w.scale, all_rows(1, H, 128), w.name)
