@@ -96,6 +96,18 @@ def bench_config(w, world: int) -> dict:
                 "flops": "4 d per visible (query, key) pair"} if w.masked else {})}
 
 
+def algorithmic_bytes(w) -> float:
+    """Q, K, V read and O written once (bf16), LSE written once (fp32)."""
+    return 2.0 * 4 * w.B * w.H * w.N * w.d + 4.0 * w.B * w.H * w.N
+
+
+def hbm_side(w, ms_step: float) -> dict:
+    peak, src = measured_peak("hbm_gbs")
+    gbs = algorithmic_bytes(w) / (ms_step * 1e-3) / 1e9
+    return {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+            "bytes_per_step": algorithmic_bytes(w), "peak_source": src}
+
+
 def rank_workload(w, rank: int):
     """Every rank solves its own problem: the same shapes, its own seed."""
     return w.with_(seed=w.seed + 1000 * rank)
@@ -790,6 +802,9 @@ def main():
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": recorded_traffic(w.name) if n_splits < 0 else None,
                     "peak_source": peak_src, "kernel": KERNEL_NAME if n_splits < 0 else KERNEL_NAME + " + merge",
+                    # the HBM side of the same launch: algorithmic bytes (Q, K, V read, O and LSE
+                    # written once) over the step time, against the measured copy bandwidth
+                    "hbm": hbm_side(w, ms_step),
                     # registers, shared memory, CTAs per SM and TMEM columns, from the runtime
                     "resources": fa.fa_kernel_resources(
                         w.d, fa.FA_KERNEL_FWD_MASKED if w.masked else
