@@ -821,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // mask keys past the diagonal (causal) and past the end of the sequence
                     int lim = p.N - 1 - (w.j0 + j) * kBlockN;
                     if (p.causal && w.j0 + j == w.qt) lim = min(lim, row);
-                    if (lim < kBlockN - 1) {
+                    if (__builtin_expect(lim < kBlockN - 1, 0)) {
                         masked = true;
 #pragma unroll
                         for (int i = 0; i < kBlockN; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
@@ -833,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int k0 = (w.j0 + j) * kBlockN;
                     const int first = row_lo - k0;
                     const int last = min(row_hi, p.N - 1) - k0;
-                    if (first > 0 || last < kBlockN - 1) {
+                    if (__builtin_expect(first > 0 || last < kBlockN - 1, 0)) {
                         masked = true;
 #pragma unroll
                         for (int i = 0; i < kBlockN; ++i) s[i] = (i < first || i > last) ? -INFINITY : s[i];
@@ -841,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // the row maximum: from the load, unless a key of the row is masked here
                 float row_max = ld_max;
-                if (__any_sync(0xffffffffu, masked)) {
+                if (__builtin_expect(__any_sync(0xffffffffu, masked), 0)) {
                     float mx[4] = {fmax3(s[0], s[1], s[2]), fmax3(s[3], s[4], s[5]), fmax3(s[6], s[7], s[8]),
                                    fmax3(s[9], s[10], s[11])};
 #pragma unroll
@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                 }
                 tmem_st64(t_lane + L::col_p(b), pk);
-                if (j > 0 && any_move) {
+                if (__builtin_expect(j > 0 && any_move, 0)) {
                     // O must hold P_{g-1} V_{g-1} before it is rescaled; one load and
                     // one store of the whole row (P is already out of the registers)
                     if (!fa_wait_warp(bar(L::kBarPVDone + (b ^ 1)), (uint32_t)(((g - 1) >> 1) & 1), abort_flag,
@@ -923,8 +923,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld128_wait(t_lane + L::kColO, r);
                     else
                         tmem_ld64_wait(t_lane + L::kColO, r);
+                    {
+                        const uint64_t a2 = f32x2_pack(a_o, a_o);
 #pragma unroll
-                    for (int i = 0; i < D; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a_o);
+                        for (int i = 0; i < D / 2; ++i) {
+                            float x0, x1;
+                            f32x2_unpack(fmul2(f32x2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), a2), x0,
+                                         x1);
+                            r[2 * i] = __float_as_uint(x0);
+                            r[2 * i + 1] = __float_as_uint(x1);
+                        }
+                    }
                     if constexpr (D == 128)
                         tmem_st128(t_lane + L::kColO, r);
                     else
