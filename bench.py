@@ -799,16 +799,20 @@ def main():
     if rank == 0:
         peak, peak_src = measured_peak()
         achieved = flops / (ms_step * 1e-3) / 1e12
+        # which forward kernel ran: masked, split-KV, or fa_fwd's choice (one CTA per
+        # query tile, or CTA pairs at d = 128)
+        fwd_kind = (fa.FA_KERNEL_FWD_MASKED if w.masked else fa.FA_KERNEL_FWD_SPLITKV if n_splits > 0
+                    else fa.fa_fwd_kernel_for(w.B, w.H, w.N, w.d, w.causal))
+        kernel_label = KERNEL_NAME + (" (CTA pairs, cta_group::2)" if fwd_kind == fa.FA_KERNEL_FWD_PAIR else
+                                      " + merge" if n_splits > 0 else "")
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": recorded_traffic(w.name) if n_splits < 0 else None,
-                    "peak_source": peak_src, "kernel": KERNEL_NAME if n_splits < 0 else KERNEL_NAME + " + merge",
+                    "peak_source": peak_src, "kernel": kernel_label,
                     # the HBM side of the same launch: algorithmic bytes (Q, K, V read, O and LSE
                     # written once) over the step time, against the measured copy bandwidth
                     "hbm": hbm_side(w, ms_step),
                     # registers, shared memory, CTAs per SM and TMEM columns, from the runtime
-                    "resources": fa.fa_kernel_resources(
-                        w.d, fa.FA_KERNEL_FWD_MASKED if w.masked else
-                        (fa.FA_KERNEL_FWD_SPLITKV if n_splits > 0 else fa.FA_KERNEL_FWD))}
+                    "resources": fa.fa_kernel_resources(w.d, fwd_kind)}
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, q, k, v)

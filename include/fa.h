@@ -372,8 +372,11 @@ int fa_watchdog_selftest_fwd(uint64_t ns, const void* q, const void* k, const vo
  * computation (the pages' "LLM kernels 3: attention and online softmax"
  * reports the same figures for its kernels).
  *
- *   kernel : FA_KERNEL_FWD (fa_fwd, fa_fwd_host), FA_KERNEL_FWD_MASKED,
- *            FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ, FA_KERNEL_BWD_DKDV.
+ *   kernel : FA_KERNEL_FWD (fa_fwd, fa_fwd_host: one CTA per query tile),
+ *            FA_KERNEL_FWD_PAIR (the same at d = 128 in CTA pairs; see
+ *            fa_set_fwd_pairing; d = 64 gives FA_ERR_HEAD_DIM),
+ *            FA_KERNEL_FWD_MASKED, FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ,
+ *            FA_KERNEL_BWD_DKDV.
  *
  * Returns FA_OK, FA_ERR_NULL_POINTER, FA_ERR_HEAD_DIM, FA_ERR_SHAPE for an
  * unknown kernel, FA_ERR_DEVICE or FA_ERR_CUDA.
@@ -383,7 +386,8 @@ enum {
     FA_KERNEL_FWD_MASKED = 1,
     FA_KERNEL_FWD_SPLITKV = 2,
     FA_KERNEL_BWD_DQ = 3,
-    FA_KERNEL_BWD_DKDV = 4
+    FA_KERNEL_BWD_DKDV = 4,
+    FA_KERNEL_FWD_PAIR = 5
 };
 typedef struct {
     int registers_per_thread;
@@ -395,6 +399,34 @@ typedef struct {
     int tmem_columns;
 } fa_kernel_resources_t;
 int fa_kernel_resources(int d, int kernel, fa_kernel_resources_t* out);
+
+/*
+ * Forward kernel choice at d = 128 for full and causal attention (fa_fwd,
+ * fa_fwd_host, and fa_fwd_masked without windows or documents).  Same results
+ * either way, up to rounding order; the choice is a matter of speed.
+ *
+ *   FA_PAIR_AUTO (default): two-CTA clusters (FA_KERNEL_FWD_PAIR) for full
+ *       attention, and for causal attention with at least 96 query tiles
+ *       (N > 12160); one CTA per query tile (FA_KERNEL_FWD) otherwise.
+ *   FA_PAIR_OFF, FA_PAIR_ON: always the one, always the other.
+ *
+ * In the pair kernel two CTAs on two SMs take adjacent query tiles against the
+ * same key tiles with two-SM tensor-core products, each SM loading half of
+ * every K and V tile; in causal attention the pair also computes the key tile
+ * after the first tile's diagonal, fully masked for that tile, which costs
+ * 1 / (key tiles + 1) of the work and is why short causal sequences keep the
+ * one-CTA kernel.  Applies to launches enqueued after the call, process-wide.
+ * Returns the previous mode, or FA_ERR_SHAPE for an unknown one.
+ */
+enum { FA_PAIR_AUTO = 0, FA_PAIR_OFF = 1, FA_PAIR_ON = 2 };
+int fa_set_fwd_pairing(int mode);
+
+/*
+ * The forward kernel fa_fwd launches for these sizes under the current mode:
+ * FA_KERNEL_FWD or FA_KERNEL_FWD_PAIR; FA_ERR_HEAD_DIM or FA_ERR_SHAPE for
+ * sizes fa_fwd rejects.  No device is touched.
+ */
+int fa_fwd_kernel_for(int B, int H, int N, int d, int causal);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int fa_version(void);

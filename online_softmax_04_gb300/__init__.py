@@ -34,7 +34,8 @@ FA_ERR_WORKSPACE = -11
 FA_ERR_SCRATCH_LIMIT = -12
 FA_ERR_MASK = -13
 FA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
-FA_KERNEL_FWD, FA_KERNEL_FWD_MASKED, FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ, FA_KERNEL_BWD_DKDV = range(5)
+FA_KERNEL_FWD, FA_KERNEL_FWD_MASKED, FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ, FA_KERNEL_BWD_DKDV, FA_KERNEL_FWD_PAIR = range(6)
+FA_PAIR_AUTO, FA_PAIR_OFF, FA_PAIR_ON = range(3)
 
 
 class KernelResources(ctypes.Structure):
@@ -100,6 +101,10 @@ def lib() -> ctypes.CDLL:
             L.fa_watchdog_selftest_fwd.restype = I
             L.fa_kernel_resources.argtypes = [I, I, ctypes.POINTER(KernelResources)]
             L.fa_kernel_resources.restype = I
+            L.fa_set_fwd_pairing.argtypes = [I]
+            L.fa_set_fwd_pairing.restype = I
+            L.fa_fwd_kernel_for.argtypes = [I, I, I, I, I]
+            L.fa_fwd_kernel_for.restype = I
             L.fa_version.argtypes = []
             L.fa_version.restype = I
             _lib = L
@@ -385,6 +390,22 @@ def fa_kernel_resources(d: int, kernel: int = FA_KERNEL_FWD) -> dict:
     if rc != FA_OK:
         raise FaError(rc, fa_strerror(rc))
     return {name: getattr(r, name) for name, _ in KernelResources._fields_}
+
+
+def fa_set_fwd_pairing(mode: int) -> int:
+    """Choose the d = 128 forward kernel (FA_PAIR_AUTO / FA_PAIR_OFF / FA_PAIR_ON); returns the previous mode."""
+    rc = int(lib().fa_set_fwd_pairing(int(mode)))
+    if rc < 0:
+        raise FaError(rc, fa_strerror(rc))
+    return rc
+
+
+def fa_fwd_kernel_for(B: int, H: int, N: int, d: int, causal: bool) -> int:
+    """FA_KERNEL_FWD or FA_KERNEL_FWD_PAIR: the kernel fa_fwd launches for these sizes."""
+    rc = int(lib().fa_fwd_kernel_for(int(B), int(H), int(N), int(d), 1 if causal else 0))
+    if rc < 0:
+        raise FaError(rc, fa_strerror(rc))
+    return rc
 
 
 def fa_version() -> int:

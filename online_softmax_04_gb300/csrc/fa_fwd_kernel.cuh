@@ -150,15 +150,21 @@ struct FaParams {
     float* ws_l32;  // fp32 sum of the exponentials
 };
 
-template <int D, int NK, int NV>
+template <int D, int NK, int NV, bool kPair = false>
 struct FaSmem {
     static_assert(D == 64 || D == 128, "head dim");
+    static_assert(!kPair || D == 128, "CTA pairs at d = 128");
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kTileBytes = kBlockN * D * 2;
+    // A CTA pair splits every K tile by keys (64 keys per CTA) and every V tile
+    // by columns (64 of d per CTA): each CTA holds half of each.
+    static constexpr uint32_t kKBytes = kPair ? kTileBytes / 2 : kTileBytes;
+    static constexpr uint32_t kVBytes = kPair ? kTileBytes / 2 : kTileBytes;
+    static constexpr uint32_t kKChunkBytes = kPair ? kChunkBytes / 2 : kChunkBytes;  // one 64-column chunk of a K stage
     static constexpr int kQBufs = 1;      // query tiles in flight: the next tile's Q lands early
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffK = kOffQ + kQBufs * kTileBytes;
-    static constexpr uint32_t kOffV = kOffK + NK * kTileBytes;
+    static constexpr uint32_t kOffV = kOffK + NK * kKBytes;
     // d = 64 leaves TMEM room for the row sums of P on the tensor core: the P V
     // product is widened to N = d + 16, and its B operand's second 64-column
     // block (reached through the descriptor's leading-byte offset) is a 2 KB
@@ -166,7 +172,7 @@ struct FaSmem {
     // of the same bf16 P (16 key rows x 128 bytes; any swizzle of ones is ones)
     static constexpr bool kTcSum = D == 64;
     static constexpr uint32_t kOnesBytes = kTcSum ? 2048u : 0u;
-    static constexpr uint32_t kOffOnes = kOffV + NV * kTileBytes;
+    static constexpr uint32_t kOffOnes = kOffV + NV * kVBytes;
     static constexpr uint32_t kOffBar = kOffOnes + kOnesBytes;
     static constexpr int kBarQ = 0;  // per Q buffer: the tile landed
     static constexpr int kBarKFull = kBarQ + kQBufs;
@@ -207,17 +213,28 @@ struct FaSmem {
     static_assert(256 + D + kSumCols + 128 <= kTmemCols, "TMEM budget");
 };
 
+// One poll of a barrier phase; kCl: with cluster-scope acquire (barriers the
+// other CTA of a pair arrives on, directly or through a tensor-core commit).
+template <bool kCl>
+__device__ __forceinline__ bool fa_poll(uint32_t bar, uint32_t parity) {
+    if constexpr (kCl)
+        return mbar_try_wait_cluster(bar, parity);
+    else
+        return mbar_try_wait(bar, parity);
+}
+
 // Bounded wait on an mbarrier phase.  Gives up when another warp of the CTA
 // has raised the abort flag, or after `limit_ns`, in which case it raises the
 // flag and records `code` in the device status word.
+template <bool kCl = false>
 __device__ __forceinline__ bool fa_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns,
                                         unsigned int code) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (fa_poll<kCl>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (fa_poll<kCl>(bar, parity)) return true;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
@@ -228,20 +245,22 @@ __device__ __forceinline__ bool fa_wait(uint32_t bar, uint32_t parity, volatile 
 }
 
 // Same, with the verdict made uniform across the warp.
+template <bool kCl = false>
 __device__ __forceinline__ bool fa_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              uint64_t limit_ns, unsigned int code) {
-    const bool ok = fa_wait(bar, parity, abort_flag, limit_ns, code);
+    const bool ok = fa_wait<kCl>(bar, parity, abort_flag, limit_ns, code);
     return __all_sync(0xffffffffu, ok);
 }
 
 // Bounded wait used while tearing down after an abort: ignores the flag.
+template <bool kCl = false>
 __device__ __forceinline__ bool fa_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (fa_poll<kCl>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (fa_poll<kCl>(bar, parity)) return true;
         if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(&g_fa_status, kStatusDrain);
             return false;
@@ -286,16 +305,23 @@ struct TileWork {
 // that CTAs take one at a time from a global counter -- first all their long
 // tiles, then the short ones -- so that CTAs that ran faster do more of the
 // tail.
-__host__ __device__ inline long long persistent_pairs(const FaParams& p) {
-    return (long long)p.BH * ((p.n_tiles + 1) / 2);
+//
+// A CTA pair schedules units of two adjacent query tiles (2u in the leading
+// CTA, 2u + 1 in its peer) the same way, the pair counting as one worker.
+__host__ __device__ inline int schedule_units(const FaParams& p, bool pair) {
+    return pair ? (p.n_tiles + 1) / 2 : p.n_tiles;
 }
 
-__device__ inline void pair_tiles(const FaParams& p, long long pair, int& bh, int& qt_long, int& qt_short) {
-    const int per_head = (p.n_tiles + 1) / 2;
+__host__ __device__ inline long long persistent_pairs(const FaParams& p, bool pair = false) {
+    return (long long)p.BH * ((schedule_units(p, pair) + 1) / 2);
+}
+
+__device__ inline void pair_tiles(int n_units, long long pair, int& bh, int& qt_long, int& qt_short) {
+    const int per_head = (n_units + 1) / 2;
     bh = (int)(pair / per_head);
     const int i = (int)(pair % per_head);
-    qt_long = p.n_tiles - 1 - i;
-    qt_short = i;  // equal to qt_long for the middle tile of an odd count
+    qt_long = n_units - 1 - i;
+    qt_short = i;  // equal to qt_long for the middle unit of an odd count
 }
 
 // Document boundaries by binary search over non-decreasing ids (indices stay
@@ -358,15 +384,20 @@ __device__ inline void tile_work(const FaParams& p, int bh, int qt, TileWork& w)
 //    works out their key ranges (tile_work()) and posts both in a
 //    shared-memory ring (produce()); the other roles read them from there
 //    (next()).  A negative entry ends the sequence.
-template <bool kSplit, bool kPersistent, bool kMask>
+//  * CTA pair: the leading CTA's producer chooses each unit and posts it in
+//    both CTAs' rings; every reader of either CTA releases the slot on the
+//    leading CTA's barrier.  Each CTA reads the unit as its own query tile.
+template <bool kSplit, bool kPersistent, bool kMask, bool kPair = false>
 struct TileSeq {
     int n = 0;               // items taken so far
     volatile int* ring;      // item ring in shared memory, 4 ints per entry
     uint32_t bar_full, bar_empty;
     volatile int* abort_flag;
     uint64_t limit;
+    uint32_t rank;           // rank in the CTA pair (0 without pairs)
     __device__ TileSeq(volatile int* ring_, uint32_t full, uint32_t empty, volatile int* abort_, uint64_t limit_)
-        : ring(ring_), bar_full(full), bar_empty(empty), abort_flag(abort_), limit(limit_) {}
+        : ring(ring_), bar_full(full), bar_empty(empty), abort_flag(abort_), limit(limit_),
+          rank(kPair ? cluster_ctarank() : 0u) {}
 
     __device__ bool one_shot(const FaParams& p, TileWork& w) {
         if (n > 0) return false;
@@ -387,16 +418,19 @@ struct TileSeq {
     // producer (one thread): choose the next tile and post it
     int round = 0, sub = 0;  // static phase: pair round and tile within the pair
     __device__ bool choose(const FaParams& p, int& bh, int& qt) {
+        const int nu = schedule_units(p, kPair);
+        const unsigned worker = kPair ? blockIdx.x >> 1 : blockIdx.x;
+        const unsigned workers = kPair ? gridDim.x >> 1 : gridDim.x;
         if (p.static_rounds < 0) {
-            // one CTA per tile: no pairing or counter needed
+            // one worker per unit: no pairing or counter needed
             if (round++ > 0) return false;
-            bh = (int)(blockIdx.x / (unsigned)p.n_tiles);
-            qt = p.n_tiles - 1 - (int)(blockIdx.x % (unsigned)p.n_tiles);
+            bh = (int)(worker / (unsigned)nu);
+            qt = nu - 1 - (int)(worker % (unsigned)nu);
             return true;
         }
         while (round < p.static_rounds) {
             int ql, qs;
-            pair_tiles(p, (long long)blockIdx.x + (long long)round * gridDim.x, bh, ql, qs);
+            pair_tiles(nu, (long long)worker + (long long)round * workers, bh, ql, qs);
             if (sub == 0 || (sub == 1 && qs != ql)) {
                 qt = sub == 0 ? ql : qs;
                 ++sub;
@@ -405,13 +439,13 @@ struct TileSeq {
             sub = 0;
             ++round;
         }
-        const long long first = (long long)p.static_rounds * gridDim.x;  // first dynamic pair
-        const long long n_dyn = persistent_pairs(p) - first;
+        const long long first = (long long)p.static_rounds * workers;  // first dynamic pair
+        const long long n_dyn = persistent_pairs(p, kPair) - first;
         for (;;) {
             const long long k = (long long)atomicAdd(p.queue, 1u);
             if (k >= 2 * n_dyn) return false;
             int ql, qs;
-            pair_tiles(p, first + (k < n_dyn ? k : k - n_dyn), bh, ql, qs);
+            pair_tiles(nu, first + (k < n_dyn ? k : k - n_dyn), bh, ql, qs);
             if (k < n_dyn) {
                 qt = ql;
                 return true;
@@ -429,15 +463,34 @@ struct TileSeq {
         } else {
             const int s = n % kItemRing;
             if (n >= kItemRing &&
-                !fa_wait(bar_empty + 8u * s, (uint32_t)(((n - kItemRing) / kItemRing) & 1), abort_flag, limit,
-                         kStatusItemWait))
+                !fa_wait<kPair>(bar_empty + 8u * s, (uint32_t)(((n - kItemRing) / kItemRing) & 1), abort_flag, limit,
+                                kStatusItemWait))
                 return false;
             int bh = 0, qt = 0;
             const bool more = choose(p, bh, qt);
-            if (more) tile_work<kMask>(p, bh, qt, w);  // the key range is worked out once, here
-            ring[4 * s + 0] = more ? bh * p.n_tiles + qt : -1;
-            ring[4 * s + 1] = more ? w.j0 : 0;
-            ring[4 * s + 2] = more ? w.n_kv : 0;
+            if (more) {
+                if constexpr (kPair) {
+                    // unit qt: query tiles 2 qt (here) and 2 qt + 1 (peer) against every
+                    // key tile either of them sees
+                    w.qt = 2 * qt;
+                    w.bh = bh;
+                    w.j0 = 0;
+                    w.n_kv = p.causal ? min(2 * qt + 2, p.n_tiles) : p.n_tiles;
+                } else {
+                    tile_work<kMask>(p, bh, qt, w);  // the key range is worked out once, here
+                }
+            }
+            const int e0 = more ? bh * schedule_units(p, kPair) + qt : -1, e1 = more ? w.j0 : 0, e2 = more ? w.n_kv : 0;
+            ring[4 * s + 0] = e0;
+            ring[4 * s + 1] = e1;
+            ring[4 * s + 2] = e2;
+            if constexpr (kPair) {
+                const uint32_t peer = mapa_shared(smem_u32(const_cast<int*>(ring + 4 * s)), 1);
+                st_cluster_u32(peer + 0, (uint32_t)e0);
+                st_cluster_u32(peer + 4, (uint32_t)e1);
+                st_cluster_u32(peer + 8, (uint32_t)e2);
+                mbar_arrive_cluster(mapa_shared(bar_full + 8u * s, 1));  // release: the peer's entry is visible
+            }
             mbar_arrive(bar_full + 8u * s);  // release: the ring entry is visible to the readers
             ++n;
             return more;
@@ -452,20 +505,22 @@ struct TileSeq {
         } else {
             const int s = n % kItemRing;
             const uint32_t par = (uint32_t)((n / kItemRing) & 1);
-            const bool ok = kWarp ? fa_wait_warp(bar_full + 8u * s, par, abort_flag, limit, kStatusItemWait)
-                                  : fa_wait(bar_full + 8u * s, par, abort_flag, limit, kStatusItemWait);
+            const bool ok = kWarp ? fa_wait_warp<kPair>(bar_full + 8u * s, par, abort_flag, limit, kStatusItemWait)
+                                  : fa_wait<kPair>(bar_full + 8u * s, par, abort_flag, limit, kStatusItemWait);
             if (!ok) return false;
             const int item = ring[4 * s + 0], j0 = ring[4 * s + 1], n_kv = ring[4 * s + 2];
-            if constexpr (kWarp) {
-                __syncwarp();
-                if ((threadIdx.x & 31) == 0) mbar_arrive(bar_empty + 8u * s);
-            } else {
-                mbar_arrive(bar_empty + 8u * s);
+            if constexpr (kWarp) __syncwarp();  // every lane has read the entry
+            if (!kWarp || (threadIdx.x & 31) == 0) {
+                if constexpr (kPair)
+                    mbar_arrive_cluster(mapa_shared(bar_empty + 8u * s, 0));  // the leading CTA's slot
+                else
+                    mbar_arrive(bar_empty + 8u * s);
             }
             ++n;
             if (item < 0) return false;
-            w.qt = item % p.n_tiles;
-            w.bh = item / p.n_tiles;
+            const int nu = schedule_units(p, kPair);
+            w.qt = kPair ? 2 * (item % nu) + (int)rank : item % nu;
+            w.bh = item / nu;
             w.j0 = j0;
             w.n_kv = n_kv;
             return true;
@@ -480,12 +535,22 @@ struct TileSeq {
 // kPersistent: one CTA per SM walks a list of tiles; the TMA ring, the S and P
 // double buffers and all barrier phases continue across tile boundaries, so
 // the loads and first S products of the next tile overlap the end of this one.
-template <int D, int NK, int NV, bool kSplit, bool kPersistent, bool kMask = false>
+// kPair: launched in clusters of two CTAs on two SMs that work on adjacent
+// query tiles 2u and 2u + 1 against the same key tiles.  Both products are
+// two-SM (cta_group::2, M = 256) products issued by the leading CTA (rank 0):
+// each CTA loads its own Q tile and half of every K tile (64 keys) and V tile
+// (64 of d), and the tensor cores of the pair exchange the halves, so each SM
+// moves half the K/V bytes per step.  Each CTA keeps its own S, P and O in its
+// own TMEM and runs its own softmax and epilogue; the barriers the leading
+// CTA's issuers wait on collect arrivals from both CTAs, and the commits of
+// the products arrive on both CTAs' barriers.  tm_k's box is 64 rows.
+template <int D, int NK, int NV, bool kSplit, bool kPersistent, bool kMask = false, bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const FaParams p) {
-    using L = FaSmem<D, NK, NV>;
-    using Seq = TileSeq<kSplit, kPersistent, kMask>;
+    static_assert(!kPair || (kPersistent && !kSplit && !kMask), "CTA pairs run the persistent unmasked kernel");
+    using L = FaSmem<D, NK, NV, kPair>;
+    using Seq = TileSeq<kSplit, kPersistent, kMask, kPair>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -497,6 +562,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = (int)(threadIdx.x & 31);
     const uint64_t limit = p.watchdog_ns;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: this CTA issues the products
+    // Arrivals the leading CTA's issuers wait for, on its barrier i (through its
+    // shared::cluster address, looked up once).  These barriers, the ones the
+    // products' commits arrive on and the waits on all of them are CTA-scope
+    // operations even across the pair: what they order is tensor-memory and
+    // operand traffic of the tcgen05 products, which the tcgen05 fences around
+    // them order (a cluster-scope release or acquire on every step measured
+    // 1.6x slower).  Data passed through shared memory between the CTAs (the
+    // work-item ring) uses cluster-scope release and acquire.
+    const uint32_t lead_bar0 = kPair ? mapa_shared(bar(0), 0) : 0u;
+    auto arrive_lead = [&](int i) {
+        if constexpr (kPair)
+            mbar_arrive_remote(lead_bar0 + 8u * (uint32_t)i);
+        else
+            mbar_arrive(bar(i));
+    };
+    // commit of this thread's products to the barrier in both CTAs of a pair
+    auto commit_all = [&](uint32_t b) {
+        if constexpr (kPair)
+            tc_commit_pair(b, (uint16_t)3);
+        else
+            tc_commit(b);
+    };
+    constexpr int kArrivers = kPair ? 2 : 1;  // CTAs whose warps arrive on the issuers' barriers
 
     if (warp == 0 && lane == 0) {
 #pragma unroll
@@ -517,13 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::kBarSFull + b), 1);
-            mbar_init(bar(L::kBarSFree + b), kSoftmaxWarps / 2);  // one arrival per warp of group b
-            mbar_init(bar(L::kBarPFull + b), kSoftmaxWarps / 2);
+            mbar_init(bar(L::kBarSFree + b), kArrivers * kSoftmaxWarps / 2);  // one arrival per warp of group b
+            mbar_init(bar(L::kBarPFull + b), kArrivers * kSoftmaxWarps / 2);
             mbar_init(bar(L::kBarPVDone + b), 1);
             mbar_init(bar(L::kBarDrain + b), 1);
         }
         mbar_init(bar(L::kBarOFinal), 1);
-        mbar_init(bar(L::kBarOFree), kSoftmaxWarps);
+        mbar_init(bar(L::kBarOFree), kArrivers * kSoftmaxWarps);
 #pragma unroll
         for (int i = 0; i < 8; ++i) mbar_init(bar(L::kBarXRef + i), 1);  // the handing-over warp
 #pragma unroll
@@ -531,7 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kItemRing; ++i) {
             mbar_init(bar(L::kBarItemFull + i), 1);
-            mbar_init(bar(L::kBarItemEmpty + i), kItemReaders);
+            // a pair's peer reads with its producer warp and softmax warps (no issuers)
+            mbar_init(bar(L::kBarItemEmpty + i), kItemReaders + (kPair ? kItemReaders - 1 : 0));
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -540,8 +630,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_v);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish();
+        }
     }
     if constexpr (L::kTcSum) {
         // the tile of ones (bf16 1.0 pairs) that the row-sum products read
@@ -551,6 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
+    // a pair: the peer's barriers are initialised before anything arrives on them
+    if constexpr (kPair) cluster_sync_all();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
@@ -562,47 +659,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------
         if (lane == 0) {
             int nk = 0, nv = 0, nq = 0;  // loads issued, over the whole tile sequence
+            // A pair's loads all complete on the leading CTA's barriers, which its
+            // producer arms with both CTAs' bytes.
+            const bool arm = !kPair || rank == 0;
+            auto full_bar = [&](uint32_t b) -> uint32_t { return kPair ? mapa_shared(b, 0) : b; };
+            auto tma = [&](uint32_t dst, const CUtensorMap* m, uint32_t b, int c0, int c1, int c2) {
+                if constexpr (kPair)
+                    tma_load_3d_pair(dst, m, b, c0, c1, c2);
+                else
+                    tma_load_3d(dst, m, b, c0, c1, c2);
+            };
             auto load_k = [&](const TileWork& w, int j) -> bool {
                 const int s = nk % NK;
                 const uint32_t r = (uint32_t)(nk / NK);
                 const uint32_t empty = bar((L::kKEmptyIsSFull ? L::kBarSFull : L::kBarKEmpty) + s);
                 if (!fa_wait(empty, (r & 1u) ^ 1u, abort_flag, limit, kStatusLoadWait)) return false;
-                mbar_arrive_expect_tx(bar(L::kBarKFull + s), L::kTileBytes);
+                if (arm) mbar_arrive_expect_tx(bar(L::kBarKFull + s), kArrivers * L::kKBytes);
+                const uint32_t fb = full_bar(bar(L::kBarKFull + s));
+                // a pair: keys 64 rank .. 64 rank + 63 of the tile
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kOffK + s * L::kTileBytes + c * kChunkBytes, &tm_k, bar(L::kBarKFull + s),
-                                c * 64, (w.j0 + j) * kBlockN, w.bh);
+                    tma(sbase + L::kOffK + s * L::kKBytes + c * L::kKChunkBytes, &tm_k, fb, c * 64,
+                        (w.j0 + j) * kBlockN + (int)rank * (kBlockN / 2), w.bh);
                 ++nk;
                 return true;
             };
             auto load_v = [&](const TileWork& w, int j) -> bool {
                 const int s = nv % NV;
                 const uint32_t r = (uint32_t)(nv / NV);
-                if (!fa_wait(bar(L::kBarVEmpty + s), (r & 1u) ^ 1u, abort_flag, limit, kStatusLoadWait)) return false;
-                mbar_arrive_expect_tx(bar(L::kBarVFull + s), L::kTileBytes);
+                if (!fa_wait(bar(L::kBarVEmpty + s), (r & 1u) ^ 1u, abort_flag, limit, kStatusLoadWait))
+                    return false;
+                if (arm) mbar_arrive_expect_tx(bar(L::kBarVFull + s), kArrivers * L::kVBytes);
+                const uint32_t fb = full_bar(bar(L::kBarVFull + s));
+                if constexpr (kPair) {
+                    // columns 64 rank .. 64 rank + 63 of d
+                    tma(sbase + L::kOffV + s * L::kVBytes, &tm_v, fb, (int)rank * 64, (w.j0 + j) * kBlockN, w.bh);
+                } else {
 #pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_3d(sbase + L::kOffV + s * L::kTileBytes + c * kChunkBytes, &tm_v, bar(L::kBarVFull + s),
-                                c * 64, (w.j0 + j) * kBlockN, w.bh);
+                    for (int c = 0; c < L::kChunks; ++c)
+                        tma(sbase + L::kOffV + s * L::kVBytes + c * kChunkBytes, &tm_v, fb, c * 64,
+                            (w.j0 + j) * kBlockN, w.bh);
+                }
                 ++nv;
                 return true;
             };
             Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
             TileWork w;
             bool ok = true;
-            while (ok && seq.produce(p, w)) {
+            // the leading CTA (or a lone CTA) chooses the work; a peer reads it
+            while (ok && (arm ? seq.produce(p, w) : seq.template next<false>(p, w))) {
                 if (w.n_kv == 0) continue;
                 const int qb = nq % L::kQBufs;
                 ok = load_k(w, 0);
                 if (ok && nq >= L::kQBufs)
-                    ok = fa_wait(bar(L::kBarQFree + qb), (uint32_t)(((nq - L::kQBufs) / L::kQBufs) & 1), abort_flag,
-                                 limit, kStatusLoadWait);
+                    ok = fa_wait(bar(L::kBarQFree + qb), (uint32_t)(((nq - L::kQBufs) / L::kQBufs) & 1),
+                                        abort_flag, limit, kStatusLoadWait);
                 if (ok) {
-                    mbar_arrive_expect_tx(bar(L::kBarQ + qb), L::kTileBytes);
+                    if (arm) mbar_arrive_expect_tx(bar(L::kBarQ + qb), kArrivers * L::kTileBytes);
+                    const uint32_t fb = full_bar(bar(L::kBarQ + qb));
+                    // a pair's peer past the last tile loads a real tile; its rows are never stored
+                    const int qrow = min(w.qt, p.n_tiles - 1) * kBlockM;
 #pragma unroll
                     for (int c = 0; c < L::kChunks; ++c)
-                        tma_load_3d(sbase + L::kOffQ + qb * L::kTileBytes + c * kChunkBytes, &tm_q, bar(L::kBarQ + qb),
-                                    c * 64, w.qt * kBlockM, w.bh);
+                        tma(sbase + L::kOffQ + qb * L::kTileBytes + c * kChunkBytes, &tm_q, fb, c * 64, qrow, w.bh);
                     ++nq;
                 }
                 if (ok && w.n_kv > 1) ok = load_k(w, 1);
@@ -611,10 +730,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok && j + 2 < w.n_kv) ok = load_k(w, j + 2);
                 }
             }
-            {
+            if (arm) {
                 // let every copy already issued land before the CTA exits: after an
                 // abort some are never consumed (in a normal run these waits succeed
-                // at once)
+                // at once).  A pair's peer cannot see its own copies land; they
+                // complete on these barriers too.
                 for (int qb = 0; qb < L::kQBufs; ++qb)
                     if (nq > qb)
                         fa_wait_drain(bar(L::kBarQ + qb), (uint32_t)(((nq - 1 - qb) / L::kQBufs) & 1), limit);
@@ -632,8 +752,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_{g-2} out of that buffer.  After a tile's last S: commit QFree of
         // its Q buffer.
         // ------------------------------------------------------------------
-        {
-            constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+        if (!kPair || rank == 0) {  // a pair's peer only allocates TMEM here
+            // a pair: M = 256 (this CTA's 128 query rows, then the peer's)
+            constexpr uint32_t kIdescS = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, kBlockN, false, false);
             int g = 0, t = 0;
             Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
             TileWork w;
@@ -643,40 +764,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qb = t % L::kQBufs;
                 const uint32_t qa = sbase + L::kOffQ + (uint32_t)qb * L::kTileBytes;
                 ok = fa_wait_warp(bar(L::kBarQ + qb), (uint32_t)((t / L::kQBufs) & 1), abort_flag, limit,
-                                  kStatusMmaWaitQ);
+                                         kStatusMmaWaitQ);
                 if (p.withhold_s) break;
                 for (int j = 0; ok && j < w.n_kv; ++j, ++g) {
                     const int b = g & 1;
                     const int ks = g % NK;
                     if (g >= 2)
-                        ok = fa_wait_warp(bar(L::kBarSFree + b), (uint32_t)(((g - 2) >> 1) & 1), abort_flag, limit,
-                                          kStatusMmaWaitSFree);
+                        ok = fa_wait_warp(bar(L::kBarSFree + b), (uint32_t)(((g - 2) >> 1) & 1), abort_flag,
+                                                 limit, kStatusMmaWaitSFree);
                     ok = ok && fa_wait_warp(bar(L::kBarKFull + ks), (uint32_t)((g / NK) & 1), abort_flag, limit,
-                                            kStatusMmaWaitK);
+                                                   kStatusMmaWaitK);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    const uint32_t ka = sbase + L::kOffK + (uint32_t)ks * L::kTileBytes;
+                    const uint32_t ka = sbase + L::kOffK + (uint32_t)ks * L::kKBytes;
                     // descriptors built once; K step kk moves the start address (16-byte
                     // units, the low field) by its byte offset
                     const uint64_t qd = sdesc_sw128(qa, 16, 1024), kd = sdesc_sw128(ka, 16, 1024);
                     if (elect_one_sync()) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = ((uint32_t)(kk >> 2) * kChunkBytes + (uint32_t)(kk & 3) * 32u) >> 4;
-                            mma_ss(tmem + L::col_s(b), sdesc_add_lo(qd, off), sdesc_add_lo(kd, off), kIdescS,
-                                   kk > 0 ? 1u : 0u);
+                            const uint32_t in_row = (uint32_t)(kk & 3) * 32u;
+                            const uint32_t offq = ((uint32_t)(kk >> 2) * kChunkBytes + in_row) >> 4;
+                            const uint32_t offk = ((uint32_t)(kk >> 2) * L::kKChunkBytes + in_row) >> 4;
+                            if constexpr (kPair)
+                                mma_ss_pair(tmem + L::col_s(b), sdesc_add_lo(qd, offq), sdesc_add_lo(kd, offk), kIdescS,
+                                            kk > 0 ? 1u : 0u);
+                            else
+                                mma_ss(tmem + L::col_s(b), sdesc_add_lo(qd, offq), sdesc_add_lo(kd, offk), kIdescS,
+                                       kk > 0 ? 1u : 0u);
                         }
-                        tc_commit(bar(L::kBarSFull + b));
-                        if constexpr (!L::kKEmptyIsSFull) tc_commit(bar(L::kBarKEmpty + ks));
+                        commit_all(bar(L::kBarSFull + b));
+                        if constexpr (!L::kKEmptyIsSFull) commit_all(bar(L::kBarKEmpty + ks));
                     }
                     __syncwarp();
                 }
-                if (ok && elect_one_sync()) tc_commit(bar(L::kBarQFree + qb));  // the Q buffer may be refilled once these finish
+                if (ok && elect_one_sync()) commit_all(bar(L::kBarQFree + qb));  // the Q buffer may be refilled once these finish
                 __syncwarp();
                 ++t;
             }
             if (elect_one_sync()) {
-                tc_commit(bar(L::kBarDrain + 0));  // every MMA must finish before TMEM is released
+                // every MMA must finish before TMEM is released
+                if constexpr (kPair)
+                    tc_commit_pair(bar(L::kBarDrain + 0), (uint16_t)1);
+                else
+                    tc_commit(bar(L::kBarDrain + 0));
                 fa_wait_drain(bar(L::kBarDrain + 0), 0, limit);
             }
         }
@@ -687,8 +818,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first product of a tile (which overwrites O) also waits until the
         // softmax warps have read the previous tile's O out of TMEM.
         // ------------------------------------------------------------------
-        {
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D + L::kSumCols, false, true);
+        if (!kPair || rank == 0) {
+            // a pair: M = 256, and each CTA's V stage holds 64 of the N = d columns
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(kPair ? 2 * kBlockM : kBlockM, D + L::kSumCols, false, true);
             int g = 0, t = 0;
             Seq seq(items, bar(L::kBarItemFull), bar(L::kBarItemEmpty), abort_flag, limit);
             TileWork w;
@@ -699,35 +831,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int b = g & 1;
                     const int vs = g % NV;
                     ok = fa_wait_warp(bar(L::kBarPFull + b), (uint32_t)((g >> 1) & 1), abort_flag, limit,
-                                      kStatusMmaWaitP) &&
+                                             kStatusMmaWaitP) &&
                          fa_wait_warp(bar(L::kBarVFull + vs), (uint32_t)((g / NV) & 1), abort_flag, limit,
-                                      kStatusMmaWaitV);
+                                             kStatusMmaWaitV);
                     if (ok && j == 0 && t > 0)
                         ok = fa_wait_warp(bar(L::kBarOFree), (uint32_t)((t - 1) & 1), abort_flag, limit,
-                                          kStatusMmaWaitP);
+                                                 kStatusMmaWaitP);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    const uint32_t va = sbase + L::kOffV + (uint32_t)vs * L::kTileBytes;
+                    const uint32_t va = sbase + L::kOffV + (uint32_t)vs * L::kVBytes;
                     // second 64-column block of B: the next chunk of V (d = 128), or the
                     // ones tile for the row sums (d = 64), whose leading-byte offset from
-                    // key rows 16 kk .. 16 kk + 15 shrinks as those rows advance
+                    // key rows 16 kk .. 16 kk + 15 shrinks as those rows advance (a pair:
+                    // each CTA's 64 columns are a single block)
                     const uint64_t vd0 = sdesc_sw128(va, L::kTcSum ? sbase + L::kOffOnes - va : kChunkBytes, 1024);
                     constexpr uint32_t kStepDesc = L::kTcSum ? 128u - (128u << 16) : 128u;  // 2048 bytes per K step
                     if (elect_one_sync()) {
 #pragma unroll
-                        for (int kk = 0; kk < kBlockN / 16; ++kk)
-                            mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u,
-                                   sdesc_add_lo(vd0, (uint32_t)kk * kStepDesc), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(bar(L::kBarVEmpty + vs));
-                        tc_commit(bar(L::kBarPVDone + b));
-                        if (j + 1 == w.n_kv) tc_commit(bar(L::kBarOFinal));
+                        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                            if constexpr (kPair)
+                                mma_ts_pair(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u,
+                                            sdesc_add_lo(vd0, (uint32_t)kk * kStepDesc), kIdescPV,
+                                            (j > 0 || kk > 0) ? 1u : 0u);
+                            else
+                                mma_ts(tmem + L::kColO, tmem + L::col_p(b) + (uint32_t)kk * 8u,
+                                       sdesc_add_lo(vd0, (uint32_t)kk * kStepDesc), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        commit_all(bar(L::kBarVEmpty + vs));
+                        commit_all(bar(L::kBarPVDone + b));
+                        if (j + 1 == w.n_kv) commit_all(bar(L::kBarOFinal));
                     }
                     __syncwarp();
                 }
                 ++t;
             }
             if (elect_one_sync()) {
-                tc_commit(bar(L::kBarDrain + 1));
+                if constexpr (kPair)
+                    tc_commit_pair(bar(L::kBarDrain + 1), (uint16_t)1);
+                else
+                    tc_commit(bar(L::kBarDrain + 1));
                 fa_wait_drain(bar(L::kBarDrain + 1), 0, limit);
             }
         }
@@ -799,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if ((g & 1) != wg) continue;
                 const int b = wg;  // S and P buffer of this step
                 if (!fa_wait_warp(bar(L::kBarSFull + b), (uint32_t)((g >> 1) & 1), abort_flag, limit,
-                                  kStatusSoftmaxWaitS)) {
+                                         kStatusSoftmaxWaitS)) {
                     ok = false;
                     break;
                 }
@@ -816,11 +958,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S_g is in registers: the buffer may take S_{g+2}
                 tc_fence_before_sync();
                 __syncwarp();
-                if (elect_one_sync()) mbar_arrive(bar(L::kBarSFree + b));
+                if (elect_one_sync()) arrive_lead(L::kBarSFree + b);
                 if constexpr (!kMask) {
                     // mask keys past the diagonal (causal) and past the end of the sequence
+                    // (a pair's leading CTA also sees the key tile after its diagonal)
                     int lim = p.N - 1 - (w.j0 + j) * kBlockN;
-                    if (p.causal && w.j0 + j == w.qt) lim = min(lim, row);
+                    if (p.causal && w.j0 + j >= w.qt) lim = min(lim, row + (w.qt - w.j0 - j) * kBlockN);
                     if (__builtin_expect(lim < kBlockN - 1, 0)) {
                         masked = true;
 #pragma unroll
@@ -900,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (g >= 2) {
                     // P buffer b last fed P_{g-2} V_{g-2}: that product must have read it
                     if (!fa_wait_warp(bar(L::kBarPVDone + b), (uint32_t)(((g - 2) >> 1) & 1), abort_flag, limit,
-                                      kStatusSoftmaxWaitPV)) {
+                                             kStatusSoftmaxWaitPV)) {
                         ok = false;
                         break;
                     }
@@ -911,7 +1054,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // O must hold P_{g-1} V_{g-1} before it is rescaled; one load and
                     // one store of the whole row (P is already out of the registers)
                     if (!fa_wait_warp(bar(L::kBarPVDone + (b ^ 1)), (uint32_t)(((g - 1) >> 1) & 1), abort_flag,
-                                      limit, kStatusSoftmaxWaitPV)) {
+                                             limit, kStatusSoftmaxWaitPV)) {
                         tmem_st_wait();  // the P store must complete before the CTA tears down
                         ok = false;
                         break;
@@ -947,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (elect_one_sync()) mbar_arrive(bar(L::kBarPFull + b));
+                if (elect_one_sync()) arrive_lead(L::kBarPFull + b);
             }
             if (!ok) break;
             // whole-row state: both groups' sums brought to the later (larger) reference.
@@ -1002,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O has been read out of TMEM: the next tile's first P V may overwrite it
                 tc_fence_before_sync();
                 __syncwarp();
-                if (elect_one_sync()) mbar_arrive(bar(L::kBarOFree));
+                if (elect_one_sync()) arrive_lead(L::kBarOFree);
             } else {
                 // this thread's half row of O in one load; the next tile's first P V
                 // may overwrite O as soon as it is in registers
@@ -1013,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32_wait(o_col, r);
                 tc_fence_before_sync();
                 __syncwarp();
-                if (elect_one_sync()) mbar_arrive(bar(L::kBarOFree));
+                if (elect_one_sync()) arrive_lead(L::kBarOFree);
                 // O/l -> bf16, straight from registers to the half row: 32-byte
                 // stores when O is 32-byte aligned (full L2 sectors), else 16-byte.
                 // (Staging through shared memory for coalesced or tensor stores
@@ -1058,9 +1201,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kPair) {
+        // Neither CTA of a pair leaves while the other may still use it.  After an
+        // abort the peer's copies may still be in flight with nothing left to wait
+        // on: they are given a millisecond (copies take microseconds) first.
+        if (threadIdx.x == 0 && *abort_flag) {
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < 1000000ull) {
+            }
+        }
+        cluster_sync_all();
+    }
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem, kTmemCols);
+        else
+            tmem_dealloc(tmem, kTmemCols);
     }
     if constexpr (kPersistent) {
         // the last CTA out leaves the counter at zero for the next launch

@@ -27,7 +27,7 @@ def test_exports_every_declared_symbol(fa):
     names = declared_functions(fa.HEADER_PATH)
     assert {"fa_fwd", "fa_strerror", "fa_get_last_error", "fa_get_device_status", "fa_clear_device_status",
             "fa_set_watchdog_ns", "fa_watchdog_selftest", "fa_watchdog_selftest_fwd", "fa_kernel_resources",
-            "fa_version"} <= set(names)
+            "fa_set_fwd_pairing", "fa_fwd_kernel_for", "fa_version"} <= set(names)
     raw = ctypes.CDLL(fa.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
@@ -38,6 +38,36 @@ def test_strerror_and_version(fa):
     for code in range(-9, 1):
         assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown error code"
     assert fa.fa_strerror(-1000) == "unknown error code"
+
+
+def test_fwd_pairing_policy(fa):
+    """Which d = 128 forward kernel a call takes: CTA pairs for full attention and
+    for causal attention from 96 query tiles on (the masked key tile a pair
+    computes per two query tiles costs 1 / (tiles / 2 + 1)); d = 64 always one
+    CTA per tile; the override modes; host-only, no device touched."""
+    F, P = fa.FA_KERNEL_FWD, fa.FA_KERNEL_FWD_PAIR
+    prev = fa.fa_set_fwd_pairing(fa.FA_PAIR_AUTO)
+    try:
+        assert fa.fa_fwd_kernel_for(1, 32, 16384, 128, True) == P      # 128 tiles
+        assert fa.fa_fwd_kernel_for(1, 1, 96 * 128, 128, True) == P    # 96 tiles
+        assert fa.fa_fwd_kernel_for(1, 1, 95 * 128, 128, True) == F    # 95 tiles
+        assert fa.fa_fwd_kernel_for(4, 16, 4096, 128, True) == F
+        assert fa.fa_fwd_kernel_for(1, 1, 1, 128, False) == P
+        assert fa.fa_fwd_kernel_for(4, 16, 4096, 128, False) == P
+        assert fa.fa_fwd_kernel_for(1, 8, 131072, 64, True) == F
+        assert fa.fa_fwd_kernel_for(1, 1, 4096, 64, False) == F
+        assert fa.fa_set_fwd_pairing(fa.FA_PAIR_OFF) == fa.FA_PAIR_AUTO
+        assert fa.fa_fwd_kernel_for(1, 1, 4096, 128, False) == F
+        assert fa.fa_set_fwd_pairing(fa.FA_PAIR_ON) == fa.FA_PAIR_OFF
+        assert fa.fa_fwd_kernel_for(1, 1, 256, 128, True) == P
+        assert fa.fa_fwd_kernel_for(1, 1, 256, 64, True) == F
+        assert fa.lib().fa_fwd_kernel_for(1, 1, 256, 96, 0) == fa.FA_ERR_HEAD_DIM
+        assert fa.lib().fa_fwd_kernel_for(0, 1, 256, 128, 0) == fa.FA_ERR_SHAPE
+        assert fa.lib().fa_fwd_kernel_for(300, 300, 256, 128, 0) == fa.FA_ERR_SHAPE
+        assert fa.lib().fa_set_fwd_pairing(7) == fa.FA_ERR_SHAPE
+        assert fa.fa_set_fwd_pairing(fa.FA_PAIR_AUTO) == fa.FA_PAIR_ON  # the bad mode changed nothing
+    finally:
+        fa.fa_set_fwd_pairing(prev)
 
 
 FAKE = 1 << 40  # never dereferenced: every case below fails validation first

@@ -5,6 +5,7 @@ Tolerances (bf16 inputs, fp32 accumulation, bf16 output): max |O_gpu - O_ref|
 <= 2e-2 over every checked element, and |LSE_gpu - LSE_ref| / max(1, |LSE_ref|)
 <= 1e-3 per checked row.
 """
+import contextlib
 import math
 
 import numpy as np
@@ -32,6 +33,19 @@ def fa():
     m.fa_clear_device_status()
     yield m
     assert m.fa_get_device_status() == 0, "a kernel gave up on a barrier"
+
+
+@contextlib.contextmanager
+def pairing(fa, mode):
+    """Force the d = 128 forward kernel (one CTA per tile, or CTA pairs) for the block."""
+    prev = fa.fa_set_fwd_pairing(mode)
+    try:
+        yield
+    finally:
+        fa.fa_set_fwd_pairing(prev)
+
+
+AUTO, OFF, ON = 0, 1, 2  # FA_PAIR_AUTO, FA_PAIR_OFF, FA_PAIR_ON
 
 
 def run_gpu(fa, q, k, v, causal, scale):
@@ -81,6 +95,20 @@ def test_small_shapes_every_row(fa, B, H, N, d, causal):
     compare(o, lse, q, k, v, causal, w.scale, all_rows(B, H, N), f"B{B} H{H} N{N} d{d} causal={causal}")
 
 
+@pytest.mark.parametrize("mode", [OFF, ON])
+@pytest.mark.parametrize("B,H,N,d,causal", [s for s in SMALL if s[3] == 128] + [(1, 3, 640, 128, True), (2, 2, 383, 128, False)])
+def test_small_shapes_each_d128_kernel(fa, mode, B, H, N, d, causal):
+    """Both d = 128 forward kernels on every small shape, every row: one CTA per
+    query tile, and CTA pairs (odd tile counts leave the peer of the last pair
+    past N; causal pairs compute a fully masked key tile for the first CTA)."""
+    w = wl.Workload("small", B, H, N, d, causal, "iid", 100 + N + d)
+    q, k, v = wl.make_inputs(w)
+    with pairing(fa, mode):
+        assert fa.fa_fwd_kernel_for(B, H, N, d, causal) == (fa.FA_KERNEL_FWD_PAIR if mode == ON else fa.FA_KERNEL_FWD)
+        o, lse = run_gpu(fa, q, k, v, causal, w.scale)
+    compare(o, lse, q, k, v, causal, w.scale, all_rows(B, H, N), f"mode {mode} B{B} H{H} N{N} causal={causal}")
+
+
 @pytest.mark.parametrize("name", [
     "B1-H1-N256-d64-full", "B1-H1-N256-d64-full-sorted", "B1-H1-N256-d64-full-sorted-strict",
     "B1-H1-N4096-d64-full",
@@ -92,18 +120,23 @@ def test_small_workloads_every_row(fa, name):
     compare(o, lse, q, k, v, w.causal, w.scale, wl.sample_rows(w), name)
 
 
-@pytest.mark.parametrize("name", [
-    "B4-H16-N4096-d128-causal", "B1-H32-N16384-d128-causal-late", "B1-H8-N131072-d64-causal",
+@pytest.mark.parametrize("name,mode", [
+    ("B4-H16-N4096-d128-causal", AUTO), ("B1-H32-N16384-d128-causal-late", AUTO), ("B1-H8-N131072-d64-causal", AUTO),
+    ("B4-H16-N4096-d128-causal", ON), ("B1-H32-N16384-d128-causal-late", OFF),
 ])
-def test_large_workloads_sampled_rows(fa, name):
+def test_large_workloads_sampled_rows(fa, name, mode):
+    """The full-size configurations in the kernel the default policy picks (the
+    headline in CTA pairs, B4-H16-N4096 one CTA per tile), and in the other one."""
     w = wl.WORKLOADS[name]
     q, k, v = wl.make_inputs(w)
-    o, lse = run_gpu(fa, q, k, v, w.causal, w.scale)
-    compare(o, lse, q, k, v, w.causal, w.scale, wl.sample_rows(w), name)
+    with pairing(fa, mode):
+        o, lse = run_gpu(fa, q, k, v, w.causal, w.scale)
+    compare(o, lse, q, k, v, w.causal, w.scale, wl.sample_rows(w), f"{name} mode {mode}")
 
 
-@pytest.mark.parametrize("d,causal", [(64, True), (64, False), (128, True)])
-def test_reference_moves_often(fa, d, causal):
+@pytest.mark.parametrize("d,causal,mode", [(64, True, AUTO), (64, False, AUTO), (128, True, OFF), (128, True, ON),
+                                           (128, False, AUTO)])
+def test_reference_moves_often(fa, d, causal, mode):
     """Scores that grow steeply along the keys (q = 8 N(0,1), key norms ramping
     from 0.25 to 8.25 times N(0,1)): a row's running maximum outgrows its
     reference by more than the rescale threshold on ~13% of (row, key tile)
@@ -116,8 +149,9 @@ def test_reference_moves_often(fa, d, causal):
     k = torch.from_numpy(rng.standard_normal((B, H, N, d), dtype=np.float32) * ramp[:, None]).to(torch.bfloat16)
     v = torch.from_numpy(rng.standard_normal((B, H, N, d), dtype=np.float32)).to(torch.bfloat16)
     scale = 1.0 / math.sqrt(d)
-    o, lse = run_gpu(fa, q, k, v, causal, scale)
-    compare(o, lse, q, k, v, causal, scale, all_rows(B, H, N), f"moving reference d{d} causal={causal}")
+    with pairing(fa, mode):
+        o, lse = run_gpu(fa, q, k, v, causal, scale)
+    compare(o, lse, q, k, v, causal, scale, all_rows(B, H, N), f"moving reference d{d} causal={causal} mode {mode}")
 
 
 # --------------------------------------------------------------------------
@@ -171,11 +205,18 @@ def test_deterministic_and_stream(fa):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_work_queue_across_calls_and_streams(fa):
+@pytest.mark.parametrize("mode", [AUTO, ON])
+def test_work_queue_across_calls_and_streams(fa, mode):
     """The persistent kernel takes tiles from a device work counter that every
     launch leaves at zero: back-to-back calls, and calls overlapping on two
     streams, must give exactly the results of the same calls run alone (every
-    tile's arithmetic is independent of which CTA runs it)."""
+    tile's arithmetic is independent of which CTA runs it).  ON: the d = 128
+    calls run in CTA pairs (128 two-tile units: static rounds + dynamic tail)."""
+    with pairing(fa, mode):
+        _work_queue_calls(fa)
+
+
+def _work_queue_calls(fa):
     wa = wl.Workload("qa", 2, 8, 2048, 128, True, "iid", 11)   # 256 tiles: static pairs + dynamic tail
     wb = wl.Workload("qb", 1, 4, 3000, 64, True, "iid", 12)    # ragged N, d = 64
     qa, ka, va = (t.cuda() for t in wl.make_inputs(wa))
@@ -200,14 +241,19 @@ def test_work_queue_across_calls_and_streams(fa):
         assert torch.equal(o, ro) and torch.equal(l, rl), which
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_output_alignment_and_bounds(fa, d):
+@pytest.mark.parametrize("d,mode", [(64, AUTO), (128, OFF), (128, ON)])
+def test_output_alignment_and_bounds(fa, d, mode):
     """O at a 16-byte but not 32-byte aligned address, N ragged: the same values
     as an aligned output, and nothing written outside O (rows past N are not
     stored, by row stores or tensor stores)."""
     B, H, N = 2, 3, 200
     w = wl.Workload("al", B, H, N, d, True, "iid", 13)
     q, k, v = (t.cuda() for t in wl.make_inputs(w))
+    with pairing(fa, mode):
+        _aligned_and_bounded(fa, q, k, v, B, H, N, d)
+
+
+def _aligned_and_bounded(fa, q, k, v, B, H, N, d):
     ref_o, ref_l = fa.attention(q, k, v, causal=True)
     n = B * H * N * d
     pad = 64                                    # elements of sentinel on each side
@@ -224,14 +270,15 @@ def test_output_alignment_and_bounds(fa, d):
     assert torch.all(buf[:pad + 8] == -7.0) and torch.all(buf[pad + 8 + n:] == -7.0)
 
 
-@pytest.mark.parametrize("B,H,N,d", [(1, 65535, 3, 64), (65535, 1, 40, 128)])
-def test_largest_head_count(fa, B, H, N, d):
+@pytest.mark.parametrize("B,H,N,d,mode", [(1, 65535, 3, 64, AUTO), (65535, 1, 40, 128, OFF), (65535, 1, 40, 128, ON)])
+def test_largest_head_count(fa, B, H, N, d, mode):
     """B*H at the limit the boundary accepts (65535): every (head, query tile)
     unit runs through the persistent schedule's static rounds and dynamic tail;
     sampled rows across the whole range, including the last head."""
     w = wl.Workload("maxbh", B, H, N, d, True, "iid", 99)
     q, k, v = wl.make_inputs(w)
-    o, lse = run_gpu(fa, q, k, v, True, w.scale)
+    with pairing(fa, mode):
+        o, lse = run_gpu(fa, q, k, v, True, w.scale)
     rng = np.random.default_rng(100)
     total = B * H * N
     rows = np.unique(np.concatenate([rng.integers(0, total, 600), [0, N - 1, total - N, total - 1]])).astype(np.int64)
@@ -278,17 +325,19 @@ def test_watchdog_ends_a_wait_nothing_completes(fa):
     assert fa.fa_get_last_error() == 0
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_watchdog_abort_leaves_nan_lse(fa, d):
+@pytest.mark.parametrize("d,mode", [(64, AUTO), (128, OFF), (128, ON)])
+def test_watchdog_abort_leaves_nan_lse(fa, d, mode):
     """The forward kernel's own abort path: its S products withheld, the softmax
     warps' first wait runs out; the tile's lse rows read NaN, o is not written,
-    and the context stays usable."""
+    and the context stays usable.  ON: a CTA pair, both CTAs abort (the peer's
+    query tile lies past N) and leave together."""
     N = 100
     w = wl.Workload("abort", 1, 1, N, d, False, "iid", 31)
     q, k, v = (t.cuda() for t in wl.make_inputs(w))
     o = torch.full_like(q, 3.0)
     lse = torch.full((1, 1, N), 7.0, dtype=torch.float32, device="cuda")
-    st = fa.fa_watchdog_selftest_fwd(5_000_000, q, k, v, o, lse, N, d)
+    with pairing(fa, mode):
+        st = fa.fa_watchdog_selftest_fwd(5_000_000, q, k, v, o, lse, N, d)
     # the first wait to run out names itself: the softmax's wait on S, or the P V issuer's wait on P
     assert st & ((1 << 5) | (1 << 3)), f"status {st:#x}"
     assert torch.isnan(lse).all()
@@ -305,8 +354,12 @@ def test_kernel_resources_report(fa, d):
     tensor memory, no local memory (no spills), 384 threads."""
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     assert sm >= 1
-    for kernel in (fa.FA_KERNEL_FWD, fa.FA_KERNEL_FWD_MASKED, fa.FA_KERNEL_FWD_SPLITKV, fa.FA_KERNEL_BWD_DQ,
-                   fa.FA_KERNEL_BWD_DKDV):
+    kernels = [fa.FA_KERNEL_FWD, fa.FA_KERNEL_FWD_MASKED, fa.FA_KERNEL_FWD_SPLITKV, fa.FA_KERNEL_BWD_DQ,
+               fa.FA_KERNEL_BWD_DKDV] + ([fa.FA_KERNEL_FWD_PAIR] if d == 128 else [])
+    if d == 64:
+        with pytest.raises(fa.FaError):
+            fa.fa_kernel_resources(64, fa.FA_KERNEL_FWD_PAIR)
+    for kernel in kernels:
         r = fa.fa_kernel_resources(d, kernel)
         assert r["threads_per_cta"] == 384, r
         assert r["ctas_per_sm"] == 1, r
@@ -316,14 +369,19 @@ def test_kernel_resources_report(fa, d):
         assert 150 * 1024 < r["dynamic_smem_bytes"] <= 227 * 1024, r
 
 
-@pytest.mark.parametrize("heads,d,causal", [(None, 64, False), ("sm+1", 64, False), (None, 128, True)])
+@pytest.mark.parametrize("heads,d,causal", [(None, 64, False), ("sm+1", 64, False), (None, 128, True),
+                                           ("pairs", 128, True), ("pairs+1", 128, True)])
 def test_one_tile_per_cta_boundary(fa, heads, d, causal):
     """N = 128, so each head is one query tile: as many heads as SMs gives each CTA
     its tile by index; one more head takes the persistent schedule with its work
-    counter.  Every row against the oracle."""
+    counter.  CTA pairs (N = 256, one two-tile unit per head): as many heads as
+    pairs fit on the device (one per two SMs), and one more.  Every row against
+    the oracle."""
     sm = torch.cuda.get_device_properties(0).multi_processor_count
-    H = sm + 1 if heads == "sm+1" else sm
-    w = wl.Workload(f"tiles-{H}", 1, H, 128, d, causal, "iid", 61 + H)
+    H = {"sm+1": sm + 1, "pairs": sm // 2, "pairs+1": sm // 2 + 1}.get(heads, sm)
+    N = 256 if heads and heads.startswith("pairs") else 128
+    w = wl.Workload(f"tiles-{H}", 1, H, N, d, causal, "iid", 61 + H)
     q, k, v = wl.make_inputs(w)
-    o, lse = run_gpu(fa, q, k, v, causal, w.scale)
-    compare(o, lse, q, k, v, causal, w.scale, all_rows(1, H, 128), w.name)
+    with pairing(fa, ON if N == 256 else AUTO):
+        o, lse = run_gpu(fa, q, k, v, causal, w.scale)
+    compare(o, lse, q, k, v, causal, w.scale, all_rows(1, H, N), w.name)
