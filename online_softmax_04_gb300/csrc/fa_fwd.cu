@@ -81,9 +81,9 @@ int queue_slot(unsigned int** out);
 // kSplit: one CTA per (query tile, head, key split).  Otherwise a persistent
 // grid of at most one CTA per SM walks the work items (see fa::TileSeq).
 template <int D, int NK, int NV, bool kSplit, bool kMask = false>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, fa::FaParams p, int BH,
-           cudaStream_t stream) {
-    using L = fa::FaSmem<D, NK, NV>;
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+           fa::FaParams p, int BH, cudaStream_t stream) {
+    using L = fa::FwdSmem<D, NK, NV, kSplit, false>;
     constexpr bool kPersistent = !kSplit;
     auto kern = fa::fa_fwd_sm103<D, NK, NV, kSplit, kPersistent, kMask>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
@@ -112,7 +112,7 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, 
             p.static_rounds = (int)(pairs / sms);
         }
     }
-    kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
+    kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -149,7 +149,7 @@ int pair_clusters(K kern, size_t smem) {
 template <int D, int NK, int NV>
 int launch_pair(const CUtensorMap& tq, const CUtensorMap& tk_half, const CUtensorMap& tv, fa::FaParams p,
                 cudaStream_t stream) {
-    using L = fa::FaSmem<D, NK, NV, true>;
+    using L = fa::FwdSmem<D, NK, NV, false, true>;
     auto kern = fa::fa_fwd_sm103<D, NK, NV, false, true, false, true>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
         return FA_ERR_CUDA;
@@ -180,13 +180,15 @@ int launch_pair(const CUtensorMap& tq, const CUtensorMap& tk_half, const CUtenso
     cfg.stream = stream;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tq, tk_half, tv, p) != cudaSuccess) return FA_ERR_CUDA;
+    // the pair kernel writes O from registers: its tm_o parameter is unused
+    if (cudaLaunchKernelEx(&cfg, kern, tq, tk_half, tv, tq, p) != cudaSuccess) return FA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 struct Prepared {
     CUtensorMap tq, tk, tv;
     CUtensorMap tk_half;  // K with a 64-row box (d = 128: the CTA-pair kernel)
+    CUtensorMap to;       // O with a 16-row box (d = 128: the one-CTA kernels' TMA stores)
     fa::FaParams p;
     int BH;
 };
@@ -211,11 +213,12 @@ bool use_pair(int d, int causal, int n_tiles) {
 
 template <bool kSplit, bool kMask = false>
 int launch_d(int d, const Prepared& pr, cudaStream_t s) {
-    if (d == 64) return launch<64, 6, 6, kSplit, kMask>(pr.tq, pr.tk, pr.tv, pr.p, pr.BH, s);
+    // (tm_o is read only by the kernels that stage O, at d = 128; the others get tq)
+    if (d == 64) return launch<64, 6, 6, kSplit, kMask>(pr.tq, pr.tk, pr.tv, pr.tq, pr.p, pr.BH, s);
     if constexpr (!kSplit && !kMask)
         if (use_pair(d, pr.p.causal, pr.p.n_tiles))
             return launch_pair<128, kPairNK, kPairNV>(pr.tq, pr.tk_half, pr.tv, pr.p, s);
-    return launch<128, 2, 3, kSplit, kMask>(pr.tq, pr.tk, pr.tv, pr.p, pr.BH, s);
+    return launch<128, 2, 3, kSplit, kMask>(pr.tq, pr.tk, pr.tv, kSplit ? pr.tq : pr.to, pr.p, pr.BH, s);
 }
 
 // Host-side argument validation shared by the entry points (no CUDA calls).
@@ -249,7 +252,8 @@ int prepare(const void* q, const void* k, const void* v, void* o, float* lse, in
     const int dev_rc = check_device();
     if (dev_rc != FA_OK) return dev_rc;
     if (!encode_bhnd(&out->tq, q, d, N, (int)BH) || !encode_bhnd(&out->tk, k, d, N, (int)BH) ||
-        !encode_bhnd(&out->tv, v, d, N, (int)BH) || (d == 128 && !encode_bhnd(&out->tk_half, k, d, N, (int)BH, 64u)))
+        !encode_bhnd(&out->tv, v, d, N, (int)BH) ||
+        (d == 128 && (!encode_bhnd(&out->tk_half, k, d, N, (int)BH, 64u) || !encode_bhnd(&out->to, o, d, N, (int)BH, 16u))))
         return FA_ERR_TENSOR_MAP;
     fa::FaParams& p = out->p;
     p = fa::FaParams{};
@@ -482,25 +486,24 @@ int kernel_resources(K kern, int threads, size_t dyn_smem, int tmem_cols, fa_ker
 
 template <int D, int NK, int NV>
 int fwd_resources(int kernel, fa_kernel_resources_t* out) {
-    using L = fa::FaSmem<D, NK, NV>;
     switch (kernel) {
         case FA_KERNEL_FWD:
-            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, false, true, false>, fa::kThreads, L::kAlloc,
-                                    (int)fa::kTmemCols, out);
+            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, false, true, false>, fa::kThreads,
+                                    fa::FwdSmem<D, NK, NV, false, false>::kAlloc, (int)fa::kTmemCols, out);
         case FA_KERNEL_FWD_PAIR:
             if constexpr (D == 128) {
-                using LP = fa::FaSmem<D, kPairNK, kPairNV, true>;
+                using LP = fa::FwdSmem<D, kPairNK, kPairNV, false, true>;
                 return kernel_resources(fa::fa_fwd_sm103<D, kPairNK, kPairNV, false, true, false, true>, fa::kThreads,
                                         LP::kAlloc, (int)fa::kTmemCols, out);
             } else {
                 return FA_ERR_HEAD_DIM;
             }
         case FA_KERNEL_FWD_MASKED:
-            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, false, true, true>, fa::kThreads, L::kAlloc,
-                                    (int)fa::kTmemCols, out);
+            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, false, true, true>, fa::kThreads,
+                                    fa::FwdSmem<D, NK, NV, false, false>::kAlloc, (int)fa::kTmemCols, out);
         case FA_KERNEL_FWD_SPLITKV:
-            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, true, false, false>, fa::kThreads, L::kAlloc,
-                                    (int)fa::kTmemCols, out);
+            return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, true, false, false>, fa::kThreads,
+                                    fa::FwdSmem<D, NK, NV, true, false>::kAlloc, (int)fa::kTmemCols, out);
         case FA_KERNEL_BWD_DQ:
             return kernel_resources(fa::fa_bwd_dq_sm103<D, D == 64 ? 4 : 2>, fa::kBwdThreads,
                                     fa::BwdSmem<D, D == 64 ? 4 : 2>::kAlloc, (int)fa::kTmemCols, out);

@@ -150,7 +150,7 @@ struct FaParams {
     float* ws_l32;  // fp32 sum of the exponentials
 };
 
-template <int D, int NK, int NV, bool kPair = false>
+template <int D, int NK, int NV, bool kPair = false, bool kOStage = false>
 struct FaSmem {
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(!kPair || D == 128, "CTA pairs at d = 128");
@@ -201,7 +201,12 @@ struct FaSmem {
     static constexpr uint32_t kOffItems = kOffXchg + (2 * kBlockM + 2 * 2 * 3 * kBlockM) * 4;
     static constexpr uint32_t kOffTmemSlot = kOffItems + kItemRing * 16;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
-    static constexpr uint32_t kBytes = kOffAbort + 4;
+    // kOStage: the epilogue writes O through shared memory and TMA stores, 2 KB per
+    // softmax warp (16 rows of its 64-column half of O, 128-byte swizzle, 1024-byte aligned)
+    static constexpr bool kOStaged = kOStage;
+    static constexpr uint32_t kOStageWarpBytes = 16 * 128;
+    static constexpr uint32_t kOffOStage = (kOffAbort + 4 + 1023) & ~1023u;
+    static constexpr uint32_t kBytes = kOStage ? kOffOStage + 8 * kOStageWarpBytes : kOffAbort + 4;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
     static_assert(kAlloc <= 232448u, "dynamic shared memory above the 227 KB a CTA may use");
     // TMEM columns: S0 S1 O [row sums] P0 P1
@@ -222,6 +227,11 @@ __device__ __forceinline__ bool fa_poll(uint32_t bar, uint32_t parity) {
     else
         return mbar_try_wait(bar, parity);
 }
+
+// The shared-memory layout of an instance: the epilogue stages O for TMA stores
+// in the one-CTA kernels at d = 128 that write O (not split-KV, not pairs).
+template <int D, int NK, int NV, bool kSplit, bool kPair>
+using FwdSmem = FaSmem<D, NK, NV, kPair, D == 128 && !kSplit && !kPair>;
 
 // Bounded wait on an mbarrier phase.  Gives up when another warp of the CTA
 // has raised the abort flag, or after `limit_ns`, in which case it raises the
@@ -547,9 +557,10 @@ struct TileSeq {
 template <int D, int NK, int NV, bool kSplit, bool kPersistent, bool kMask = false, bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const FaParams p) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 const FaParams p) {
     static_assert(!kPair || (kPersistent && !kSplit && !kMask), "CTA pairs run the persistent unmasked kernel");
-    using L = FaSmem<D, NK, NV, kPair>;
+    using L = FwdSmem<D, NK, NV, kSplit, kPair>;
     using Seq = TileSeq<kSplit, kPersistent, kMask, kPair>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1157,10 +1168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (elect_one_sync()) arrive_lead(L::kBarOFree);
-                // O/l -> bf16, straight from registers to the half row: 32-byte
-                // stores when O is 32-byte aligned (full L2 sectors), else 16-byte.
-                // (Staging through shared memory for coalesced or tensor stores
-                // measured slower.)
+                // O/l -> bf16
                 const float inv_l = l_fin > 0.f ? 1.f / l_fin : 0.f;
                 uint32_t wv[kOCols / 2];
 #pragma unroll
@@ -1168,7 +1176,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wv[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
                                       ((size_t)w.bh * (size_t)p.N + (size_t)q_idx) * D + wg * kOCols;
-                if (valid) {
+                if constexpr (L::kOStaged) {
+                    // Through shared memory and the TMA unit, so that the warp goes on while
+                    // the tile is written (row stores from registers kept the softmax warps
+                    // ~1700 cycles a tile): two boxes of 16 rows x 64 columns per warp, each
+                    // staged in the warp's 2 KB with the 128-byte swizzle (16-byte chunk u of
+                    // row r at chunk u ^ (r % 8)); rows past N are dropped by the tensor map.
+                    // The elected lane issues the stores and waits for its own earlier ones.
+                    const uint32_t wst = sbase + L::kOffOStage + (uint32_t)(warp - 4) * L::kOStageWarpBytes;
+                    const int row0 = w.qt * kBlockM + quarter * 32;  // sequence position of lane 0's row
+#pragma unroll
+                    for (int pass = 0; pass < 2; ++pass) {
+                        // the staging area has been read by the previous box's store
+                        if (elect_one_sync()) bulk_wait_read_all();
+                        __syncwarp();
+                        if ((lane >> 4) == pass) {
+                            const uint32_t rowa = wst + (uint32_t)(lane & 15) * 128u;
+#pragma unroll
+                            for (int u = 0; u < kOCols / 8; ++u)
+                                st_shared_v4(rowa + (uint32_t)((u ^ (lane & 7)) * 16), wv[4 * u], wv[4 * u + 1],
+                                             wv[4 * u + 2], wv[4 * u + 3]);
+                            fence_proxy_async_smem();  // visible to the TMA unit
+                        }
+                        __syncwarp();
+                        if (elect_one_sync()) {
+                            tma_store_3d(&tm_o, wst, wg * kOCols, row0 + 16 * pass, w.bh);
+                            bulk_commit_group();
+                        }
+                        __syncwarp();
+                    }
+                } else if (valid) {
+                    // straight from registers to the half row: 32-byte stores when O is
+                    // 32-byte aligned (full L2 sectors), else 16-byte
                     if ((reinterpret_cast<uintptr_t>(p.o) & 31u) == 0) {
 #pragma unroll
                         for (int u = 0; u < kOCols / 16; ++u) st_global_v8(orow + 16 * u, wv + 8 * u);
@@ -1195,6 +1234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.ws_m[((size_t)blockIdx.z * gridDim.y + (size_t)w.bh) * (size_t)p.N + (size_t)q_idx] = nan;
             else
                 p.lse[(size_t)w.bh * (size_t)p.N + (size_t)q_idx] = nan;
+        }
+        if constexpr (L::kOStaged) {
+            // this warp's O stores have completed before the CTA exits
+            if (elect_one_sync()) bulk_wait_all();
         }
         __syncwarp();
     }
