@@ -120,6 +120,28 @@ def test_small_workloads_every_row(fa, name):
     compare(o, lse, q, k, v, w.causal, w.scale, wl.sample_rows(w), name)
 
 
+def test_random_shapes_both_d128_kernels(fa):
+    """Twelve seeded random shapes (B, H, N with odd and even query-tile counts and
+    ragged tails, causal or not), each through both d = 128 forward kernels and
+    compared with the oracle on every row: the two kernels' per-row arithmetic is
+    the same, so they must also agree with each other bit for bit."""
+    rng = np.random.default_rng(20261202)
+    for case in range(12):
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+        N = int(rng.integers(1, 1400))
+        causal = bool(rng.integers(0, 2))
+        w = wl.Workload(f"rand{case}", B, H, N, 128, causal, "iid", 500 + case)
+        q, k, v = wl.make_inputs(w)
+        outs = []
+        for mode in (OFF, ON):
+            with pairing(fa, mode):
+                outs.append(run_gpu(fa, q, k, v, causal, w.scale))
+        assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1]), \
+            f"B{B} H{H} N{N} causal={causal}: the two kernels differ"
+        compare(outs[1][0], outs[1][1], q, k, v, causal, w.scale, all_rows(B, H, N),
+                f"random B{B} H{H} N{N} causal={causal}")
+
+
 @pytest.mark.parametrize("name,mode", [
     ("B4-H16-N4096-d128-causal", AUTO), ("B1-H32-N16384-d128-causal-late", AUTO), ("B1-H8-N131072-d64-causal", AUTO),
     ("B4-H16-N4096-d128-causal", ON), ("B1-H32-N16384-d128-causal-late", OFF),
