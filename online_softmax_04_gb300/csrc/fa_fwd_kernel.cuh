@@ -43,9 +43,10 @@
 //     softmax warps form two groups of four (one warp per 32-row TMEM lane
 //     quarter) that take alternate key tiles, a thread holding all 128 scores
 //     of its row.  Only the reference maximum passes from one step to the
-//     next; each group hands it to the other through shared memory as soon as
-//     its row maximum is known, so the exponentials of step j overlap the
-//     TMEM load and maximum of step j+1.  Each group keeps its row sums
+//     next; each group hands it to the other through shared memory (one
+//     64-bit word per row tagged with the step) as soon as its row maximum is
+//     known, so the exponentials of step j overlap the TMEM load and maximum of
+//     step j+1.  Each group keeps its row sums
 //     against the last reference it used; the two are combined at the end.
 //   * The reference maximum of a row moves only when the row maximum has
 //     grown past it by more than 64 in base-2 units; otherwise the old
@@ -190,15 +191,16 @@ struct FaSmem {
     static constexpr int kBarQFree = kBarOFinal + 1;   // per Q buffer: the tile's last S product finished
     static constexpr int kBarOFree = kBarQFree + kQBufs;  // per tile: O read out of TMEM (accumulator reusable)
     static constexpr int kBarDrain = kBarOFree + 1;    // per MMA issuer
-    static constexpr int kBarXRef = kBarDrain + 2;     // per lane quarter and softmax group: reference handed over
-    static constexpr int kBarXSum = kBarXRef + 8;      // per lane quarter: both groups' row sums posted
+    static constexpr int kBarXSum = kBarDrain + 2;     // per lane quarter: both groups' row sums posted
     static constexpr int kBarItemFull = kBarXSum + 4;  // per item-ring slot: the producer posted an item
     static constexpr int kBarItemEmpty = kBarItemFull + kItemRing;  // per slot: every role has read it
     static constexpr int kNumBars = kBarItemEmpty + kItemRing;
-    // references [2 groups][128 rows], then row states [2 tile parities][2 groups][m, l, l32][128 rows]
+    // reference hand-over slots [2 groups][128 rows] of (step << 32 | reference bits), then row
+    // states [2 tile parities][2 groups][m, l, l32][128 rows]
     static constexpr uint32_t kOffXchg = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kOffXSum = kOffXchg + 2 * kBlockM * 8;
     // work-item ring: per entry {bh * n_tiles + qt, first key tile, key tiles, unused}
-    static constexpr uint32_t kOffItems = kOffXchg + (2 * kBlockM + 2 * 2 * 3 * kBlockM) * 4;
+    static constexpr uint32_t kOffItems = kOffXSum + 2 * 2 * 3 * kBlockM * 4;
     static constexpr uint32_t kOffTmemSlot = kOffItems + kItemRing * 16;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
     // kOStage: the epilogue writes O through shared memory and TMA stores, 2 KB per
@@ -276,6 +278,52 @@ __device__ __forceinline__ bool fa_wait_drain(uint32_t bar, uint32_t parity, uin
             return false;
         }
     }
+}
+
+// The reference hand-over between the two softmax groups, one 64-bit shared-memory
+// word per row: the step the reference belongs to in the high half, its bits in the
+// low half.  A naturally aligned 64-bit store is single-copy atomic, so a reader that
+// sees the step it expects also sees that step's reference, with no barrier between.
+__device__ __forceinline__ void xref_put(uint32_t addr, uint32_t step, float m) {
+    const uint64_t v = ((uint64_t)step << 32) | (uint64_t)__float_as_uint(m);
+    asm volatile("st.volatile.shared.b64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// `x`, recomputed where it is used (an opaque copy the compiler cannot hoist out
+// of a loop and hold in a register across it)
+__device__ __forceinline__ uint32_t fa_here(uint32_t x) {
+    uint32_t y;
+    asm volatile("mov.b32 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint64_t xref_ld(uint32_t addr) {
+    uint64_t v;
+    asm volatile("ld.volatile.shared.b64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Bounded wait for step `step`'s reference in the slot at `addr` (watchdog as fa_wait).
+__device__ __forceinline__ bool xref_get(uint32_t addr, uint32_t step, float& m, volatile int* abort_flag,
+                                         uint64_t limit_ns) {
+    uint64_t v = xref_ld(addr);
+    if (__builtin_expect((uint32_t)(v >> 32) != step, 0)) {
+        // elapsed SM cycles in 32 bits against the limit at 2 cycles per ns (at most 2^31)
+        const uint32_t c0 = (uint32_t)clock();
+        const uint32_t lim = limit_ns >= (1ull << 30) ? (1u << 31) : (uint32_t)limit_ns * 2u;
+        for (;;) {
+            v = xref_ld(addr);
+            if ((uint32_t)(v >> 32) == step) break;
+            if (*abort_flag) return false;
+            if ((uint32_t)clock() - c0 > lim) {
+                *abort_flag = 1;
+                atomicOr(&g_fa_status, kStatusSoftmaxWaitX);
+                return false;
+            }
+        }
+    }
+    m = __uint_as_float((uint32_t)v);
+    return true;
 }
 
 // Exponentials of NE keys of a row against the reference -neg_m (base 2):
@@ -625,8 +673,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::kBarOFinal), 1);
         mbar_init(bar(L::kBarOFree), kArrivers * kSoftmaxWarps);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mbar_init(bar(L::kBarXRef + i), 1);  // the handing-over warp
-#pragma unroll
         for (int i = 0; i < 4; ++i) mbar_init(bar(L::kBarXSum + i), 2);
 #pragma unroll
         for (int i = 0; i < kItemRing; ++i) {
@@ -648,6 +694,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_alloc(smem_u32(tmem_slot), kTmemCols);
             tmem_relinquish();
         }
+    }
+    {
+        // reference hand-over slots: no step yet
+        volatile uint64_t* slots = reinterpret_cast<volatile uint64_t*>(smem + L::kOffXchg);
+        for (uint32_t i = threadIdx.x; i < 2u * kBlockM; i += blockDim.x) slots[i] = ~0ull;
     }
     if constexpr (L::kTcSum) {
         // the tile of ones (bf16 1.0 pairs) that the row-sum products read
@@ -899,8 +950,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wg = (warp - 4) >> 2;  // warps 4-7: even steps, warps 8-11: odd steps
         const int row = quarter * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        float* xref = reinterpret_cast<float*>(smem + L::kOffXchg);  // [2 groups][128 rows]
-        float* xsum = xref + 2 * kBlockM;                              // [2 tile parities][2 groups][3][128 rows]
+        // this row's hand-over slot of group gr (group 1's is 8 * 128 bytes after group 0's)
+        auto xslot = [&](int gr) -> uint32_t {
+            return fa_here(sbase) + L::kOffXchg + (uint32_t)(gr * kBlockM + row) * 8u;
+        };
+        float* xsum = reinterpret_cast<float*>(smem + L::kOffXSum);  // [2 tile parities][2 groups][3][128 rows]
         constexpr int kOCols = D / 2;  // O columns this thread stores in the epilogue
         const float c2 = p.scale_log2;
         int g = 0, t = 0;  // steps and non-empty tiles so far
@@ -1010,17 +1064,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (masked) row_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 }
                 // reference after step g-1, handed over by the other group (every step
-                // after the first waits, so the hand-overs stay in lock step; a new
+                // after the first waits for it, so the hand-overs stay in lock step; a new
                 // tile starts from -inf and ignores the value)
                 float m_prev = -INFINITY;
                 if (g > 0) {
-                    if (!fa_wait_warp(bar(L::kBarXRef + quarter * 2 + (wg ^ 1)), (uint32_t)(((g - 1) >> 1) & 1),
-                                      abort_flag, limit, kStatusSoftmaxWaitX)) {
-                        ok = false;
-                        break;
+                    const uint32_t other = xslot(wg ^ 1);
+                    uint64_t xv = xref_ld(other);
+                    if (__builtin_expect(__any_sync(0xffffffffu, (uint32_t)(xv >> 32) != (uint32_t)(g - 1)), 0)) {
+                        float v = -INFINITY;
+                        if (!__all_sync(0xffffffffu, xref_get(other, (uint32_t)(g - 1), v, abort_flag, limit))) {
+                            ok = false;
+                            break;
+                        }
+                        xv = (uint64_t)__float_as_uint(v);
                     }
-                    const float v = xref[(wg ^ 1) * kBlockM + row];
-                    if (j > 0) m_prev = v;
+                    if (j > 0) m_prev = __uint_as_float((uint32_t)xv);
                 }
                 // scale > 0, so max(s) * c2 == max(s * c2); the reference moves only
                 // when the max grew past it by more than the threshold (always on
@@ -1028,9 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_cand = fmaxf(m_prev, row_max * c2);
                 const bool move = m_cand > m_prev + kRescaleThreshold;
                 const float m_new = move ? m_cand : m_prev;
-                xref[wg * kBlockM + row] = m_new;
-                __syncwarp();
-                if (elect_one_sync()) mbar_arrive(bar(L::kBarXRef + quarter * 2 + wg));
+                xref_put(xslot(wg), (uint32_t)g, m_new);
                 const bool any_move = __any_sync(0xffffffffu, move);
                 // bring this group's sums to the new reference (its last step may be
                 // two or more moves back)
@@ -1158,22 +1214,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (elect_one_sync()) arrive_lead(L::kBarOFree);
             } else {
-                // this thread's half row of O in one load; the next tile's first P V
-                // may overwrite O as soon as it is in registers
-                uint32_t r[kOCols];
-                if constexpr (kOCols == 64)
-                    tmem_ld64_wait(o_col, r);
-                else
-                    tmem_ld32_wait(o_col, r);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (elect_one_sync()) arrive_lead(L::kBarOFree);
-                // O/l -> bf16
+                // this thread's half row of O, 32 columns at a time, O/l -> bf16 as it
+                // arrives (fewer registers live than one load of the half row); the next
+                // tile's first P V may overwrite O as soon as it is all in registers
                 const float inv_l = l_fin > 0.f ? 1.f / l_fin : 0.f;
                 uint32_t wv[kOCols / 2];
 #pragma unroll
-                for (int i = 0; i < kOCols / 2; ++i)
-                    wv[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+                for (int h = 0; h < kOCols / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld32_wait(o_col + 32u * (uint32_t)h, r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        wv[16 * h + i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (elect_one_sync()) arrive_lead(L::kBarOFree);
                 __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
                                       ((size_t)w.bh * (size_t)p.N + (size_t)q_idx) * D + wg * kOCols;
                 if constexpr (L::kOStaged) {
@@ -1183,7 +1239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // staged in the warp's 2 KB with the 128-byte swizzle (16-byte chunk u of
                     // row r at chunk u ^ (r % 8)); rows past N are dropped by the tensor map.
                     // The elected lane issues the stores and waits for its own earlier ones.
-                    const uint32_t wst = sbase + L::kOffOStage + (uint32_t)(warp - 4) * L::kOStageWarpBytes;
+                    const uint32_t wst = fa_here(sbase) + L::kOffOStage + (uint32_t)(warp - 4) * L::kOStageWarpBytes;
                     const int row0 = w.qt * kBlockM + quarter * 32;  // sequence position of lane 0's row
 #pragma unroll
                     for (int pass = 0; pass < 2; ++pass) {
