@@ -801,12 +801,13 @@ def main():
     if rank == 0:
         peak, peak_src = measured_peak()
         achieved = flops / (ms_step * 1e-3) / 1e12
-        # which forward kernel ran: masked, split-KV, or fa_fwd's choice (one CTA per
-        # query tile, or CTA pairs at d = 128)
+        # which forward kernel ran: masked, split-KV, or fa_fwd's choice (one query tile
+        # per CTA, CTA pairs at d = 128, or two tiles per CTA at d = 64)
         fwd_kind = (fa.FA_KERNEL_FWD_MASKED if w.masked else fa.FA_KERNEL_FWD_SPLITKV if n_splits > 0
                     else fa.fa_fwd_kernel_for(w.B, w.H, w.N, w.d, w.causal))
-        kernel_label = KERNEL_NAME + (" (CTA pairs, cta_group::2)" if fwd_kind == fa.FA_KERNEL_FWD_PAIR else
-                                      " + merge" if n_splits > 0 else "")
+        kernel_label = (KERNEL_NAME + " (CTA pairs, cta_group::2)" if fwd_kind == fa.FA_KERNEL_FWD_PAIR else
+                        "fa_fwd2_sm103 (two query tiles per CTA)" if fwd_kind == fa.FA_KERNEL_FWD_TWO else
+                        KERNEL_NAME + (" + merge" if n_splits > 0 else ""))
         # the burst peak is the denominator (the kernel is timed on its own); the sustained,
         # power-capped figure is given beside it: over long runs the power cap lowers the clock
         peak_sus, _ = measured_peak("bf16_tflops_sustained")

@@ -375,6 +375,8 @@ int fa_watchdog_selftest_fwd(uint64_t ns, const void* q, const void* k, const vo
  *   kernel : FA_KERNEL_FWD (fa_fwd, fa_fwd_host: one CTA per query tile),
  *            FA_KERNEL_FWD_PAIR (the same at d = 128 in CTA pairs; see
  *            fa_set_fwd_pairing; d = 64 gives FA_ERR_HEAD_DIM),
+ *            FA_KERNEL_FWD_TWO (the same at d = 64 with two query tiles
+ *            per CTA; d = 128 gives FA_ERR_HEAD_DIM),
  *            FA_KERNEL_FWD_MASKED, FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ,
  *            FA_KERNEL_BWD_DKDV.
  *
@@ -387,7 +389,8 @@ enum {
     FA_KERNEL_FWD_SPLITKV = 2,
     FA_KERNEL_BWD_DQ = 3,
     FA_KERNEL_BWD_DKDV = 4,
-    FA_KERNEL_FWD_PAIR = 5
+    FA_KERNEL_FWD_PAIR = 5,
+    FA_KERNEL_FWD_TWO = 6
 };
 typedef struct {
     int registers_per_thread;
@@ -401,30 +404,41 @@ typedef struct {
 int fa_kernel_resources(int d, int kernel, fa_kernel_resources_t* out);
 
 /*
- * Forward kernel choice at d = 128 for full and causal attention (fa_fwd,
- * fa_fwd_host, and fa_fwd_masked without windows or documents).  Same results
- * either way, up to rounding order; the choice is a matter of speed.
+ * Forward kernel choice for full and causal attention (fa_fwd, fa_fwd_host,
+ * and fa_fwd_masked without windows or documents): one query tile per CTA, or
+ * units of two adjacent query tiles.  Same results either way, up to rounding
+ * order; the choice is a matter of speed.
  *
- *   FA_PAIR_AUTO (default): two-CTA clusters (FA_KERNEL_FWD_PAIR) for full
- *       attention, and for causal attention with at least 96 query tiles
- *       (N > 12160); one CTA per query tile (FA_KERNEL_FWD) otherwise.
+ *   d = 128: units are CTA pairs (FA_KERNEL_FWD_PAIR): two CTAs on two SMs
+ *       take the two tiles against the same key tiles with two-SM tensor-core
+ *       products, each SM loading half of every K and V tile.
+ *   d = 64: units are two tiles in one CTA (FA_KERNEL_FWD_TWO), each tile with
+ *       its own softmax warpgroup, S, P and O, the K and V tiles loaded once
+ *       for both.
+ *
+ *   FA_PAIR_AUTO (default): at d = 128, CTA pairs for full attention and for
+ *       causal attention with at least 96 query tiles (N > 12160); at d = 64,
+ *       two tiles per CTA when a model of both schedules on a 152-SM GB300
+ *       (the two-tile kernel's step at 0.9 of the one-tile kernel's, half as
+ *       many units) says it finishes first, which holds once there are about
+ *       as many units as SMs (not for one head of N = 4096); one query tile
+ *       per CTA (FA_KERNEL_FWD) otherwise.
  *   FA_PAIR_OFF, FA_PAIR_ON: always the one, always the other.
  *
- * In the pair kernel two CTAs on two SMs take adjacent query tiles against the
- * same key tiles with two-SM tensor-core products, each SM loading half of
- * every K and V tile; in causal attention the pair also computes the key tile
- * after the first tile's diagonal, fully masked for that tile, which costs
- * 1 / (key tiles + 1) of the work and is why short causal sequences keep the
- * one-CTA kernel.  Applies to launches enqueued after the call, process-wide.
- * Returns the previous mode, or FA_ERR_SHAPE for an unknown one.
+ * In causal attention a unit also computes the key tile after its first
+ * tile's diagonal, fully masked for that tile, which costs 1 / (key tiles + 1)
+ * of the work and is why short causal sequences keep one tile per CTA.
+ * Applies to launches enqueued after the call, process-wide.  Returns the
+ * previous mode, or FA_ERR_SHAPE for an unknown one.
  */
 enum { FA_PAIR_AUTO = 0, FA_PAIR_OFF = 1, FA_PAIR_ON = 2 };
 int fa_set_fwd_pairing(int mode);
 
 /*
  * The forward kernel fa_fwd launches for these sizes under the current mode:
- * FA_KERNEL_FWD or FA_KERNEL_FWD_PAIR; FA_ERR_HEAD_DIM or FA_ERR_SHAPE for
- * sizes fa_fwd rejects.  No device is touched.
+ * FA_KERNEL_FWD, FA_KERNEL_FWD_PAIR (d = 128) or FA_KERNEL_FWD_TWO (d = 64);
+ * FA_ERR_HEAD_DIM or FA_ERR_SHAPE for sizes fa_fwd rejects.  No device is
+ * touched.
  */
 int fa_fwd_kernel_for(int B, int H, int N, int d, int causal);
 

@@ -34,7 +34,8 @@ FA_ERR_WORKSPACE = -11
 FA_ERR_SCRATCH_LIMIT = -12
 FA_ERR_MASK = -13
 FA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
-FA_KERNEL_FWD, FA_KERNEL_FWD_MASKED, FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ, FA_KERNEL_BWD_DKDV, FA_KERNEL_FWD_PAIR = range(6)
+(FA_KERNEL_FWD, FA_KERNEL_FWD_MASKED, FA_KERNEL_FWD_SPLITKV, FA_KERNEL_BWD_DQ, FA_KERNEL_BWD_DKDV, FA_KERNEL_FWD_PAIR,
+ FA_KERNEL_FWD_TWO) = range(7)
 FA_PAIR_AUTO, FA_PAIR_OFF, FA_PAIR_ON = range(3)
 
 
@@ -393,7 +394,8 @@ def fa_kernel_resources(d: int, kernel: int = FA_KERNEL_FWD) -> dict:
 
 
 def fa_set_fwd_pairing(mode: int) -> int:
-    """Choose the d = 128 forward kernel (FA_PAIR_AUTO / FA_PAIR_OFF / FA_PAIR_ON); returns the previous mode."""
+    """Choose the forward kernel: one query tile per CTA, or units of two tiles (CTA pairs at d = 128,
+    two tiles per CTA at d = 64); FA_PAIR_AUTO / FA_PAIR_OFF / FA_PAIR_ON.  Returns the previous mode."""
     rc = int(lib().fa_set_fwd_pairing(int(mode)))
     if rc < 0:
         raise FaError(rc, fa_strerror(rc))
@@ -401,7 +403,7 @@ def fa_set_fwd_pairing(mode: int) -> int:
 
 
 def fa_fwd_kernel_for(B: int, H: int, N: int, d: int, causal: bool) -> int:
-    """FA_KERNEL_FWD or FA_KERNEL_FWD_PAIR: the kernel fa_fwd launches for these sizes."""
+    """FA_KERNEL_FWD, FA_KERNEL_FWD_PAIR or FA_KERNEL_FWD_TWO: the kernel fa_fwd launches for these sizes."""
     rc = int(lib().fa_fwd_kernel_for(int(B), int(H), int(N), int(d), 1 if causal else 0))
     if rc < 0:
         raise FaError(rc, fa_strerror(rc))

@@ -12,6 +12,7 @@
 
 #include "../../include/fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_two_kernel.cuh"
 #include "softmax_rows.cuh"
 #include "fa_bwd_kernel.cuh"
 
@@ -185,6 +186,32 @@ int launch_pair(const CUtensorMap& tq, const CUtensorMap& tk_half, const CUtenso
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// The d = 64 persistent kernel with two query tiles per CTA (see fa::fa_fwd2_sm103).
+template <int NK, int NV>
+int launch_two(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, fa::FaParams p,
+               cudaStream_t stream) {
+    using L = fa::TwoSmem<NK, NV>;
+    auto kern = fa::fa_fwd2_sm103<NK, NV>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
+        return FA_ERR_CUDA;
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    const long long units = (long long)p.BH * fa::schedule_units(p, true);
+    unsigned grid;
+    if (units <= sms) {
+        // one CTA per unit, fixed by its index: no work counter
+        grid = (unsigned)units;
+        p.static_rounds = -1;
+        p.queue = nullptr;
+    } else {
+        const int qrc = queue_slot(&p.queue);
+        if (qrc != FA_OK) return qrc;
+        grid = (unsigned)sms;
+        p.static_rounds = (int)(fa::persistent_pairs(p, true) / sms);
+    }
+    kern<<<grid, fa::kThreads, L::kAlloc, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 struct Prepared {
     CUtensorMap tq, tk, tv;
     CUtensorMap tk_half;  // K with a 64-row box (d = 128: the CTA-pair kernel)
@@ -211,9 +238,51 @@ bool use_pair(int d, int causal, int n_tiles) {
     return !causal || n_tiles >= kPairMinCausalTiles;
 }
 
+// K and V stages (16 KB each) of the two-tile kernel
+constexpr int kTwoNK = 6, kTwoNV = 5;
+
+// The d = 64 kernel with two query tiles per CTA runs a tile step in ~0.9 of
+// the one-tile kernel's time (0.88-0.95 measured over causal and full shapes),
+// but it has half as many work units, and a causal unit also computes the key
+// tile after its first tile's diagonal.  Under FA_PAIR_AUTO it is taken when a
+// model of both schedules on a 152-SM GB300 says it finishes first: full
+// attention runs ceil(units / SMs) rounds of equal units; causal attention is
+// balanced by the long+short schedule, so its time is the steps per SM or the
+// longest unit, whichever is larger.  (Host-only: no device is queried.)
+constexpr long long kPolicySms = 152;
+
+bool use_two(int d, int causal, int n_tiles, long long BH) {
+    if (d != 64) return false;
+    const int mode = g_pairing.load();
+    if (mode == FA_PAIR_OFF) return false;
+    if (mode == FA_PAIR_ON) return true;
+    const long long n = n_tiles, units = (n + 1) / 2;
+    const double r = 0.9;  // a two-tile step against a one-tile step
+    double one, two;
+    if (!causal) {
+        one = (double)((BH * n + kPolicySms - 1) / kPolicySms) * (double)n;
+        two = r * (double)((BH * units + kPolicySms - 1) / kPolicySms) * 2.0 * (double)n;
+    } else {
+        // steps per head: query tile t sees t + 1 key tiles; unit u runs both its
+        // tiles over min(2u + 2, n) key tiles
+        const long long steps_one = n * (n + 1) / 2;
+        long long steps_two = 0;
+        for (long long u = 0; u < units; ++u) steps_two += 2 * std::min(2 * u + 2, n);
+        one = std::max((double)(BH * steps_one) / (double)kPolicySms, (double)n);
+        two = r * std::max((double)(BH * steps_two) / (double)kPolicySms, 2.0 * (double)n);
+    }
+    return two < one;
+}
+
+// two: -1 lets the policy choose the d = 64 kernel for these sizes; 0 or 1 forces
+// one tile or two tiles per CTA (a caller that splits one problem into several
+// launches decides once, for the whole problem)
 template <bool kSplit, bool kMask = false>
-int launch_d(int d, const Prepared& pr, cudaStream_t s) {
+int launch_d(int d, const Prepared& pr, cudaStream_t s, int two = -1) {
     // (tm_o is read only by the kernels that stage O, at d = 128; the others get tq)
+    if constexpr (!kSplit && !kMask)
+        if (d == 64 && (two >= 0 ? two == 1 : use_two(d, pr.p.causal, pr.p.n_tiles, pr.BH)))
+            return launch_two<kTwoNK, kTwoNV>(pr.tq, pr.tk, pr.tv, pr.p, s);
     if (d == 64) return launch<64, 6, 6, kSplit, kMask>(pr.tq, pr.tk, pr.tv, pr.tq, pr.p, pr.BH, s);
     if constexpr (!kSplit && !kMask)
         if (use_pair(d, pr.p.causal, pr.p.n_tiles))
@@ -498,6 +567,13 @@ int fwd_resources(int kernel, fa_kernel_resources_t* out) {
             } else {
                 return FA_ERR_HEAD_DIM;
             }
+        case FA_KERNEL_FWD_TWO:
+            if constexpr (D == 64) {
+                return kernel_resources(fa::fa_fwd2_sm103<kTwoNK, kTwoNV>, fa::kThreads,
+                                        fa::TwoSmem<kTwoNK, kTwoNV>::kAlloc, (int)fa::kTmemCols, out);
+            } else {
+                return FA_ERR_HEAD_DIM;
+            }
         case FA_KERNEL_FWD_MASKED:
             return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, false, true, true>, fa::kThreads,
                                     fa::FwdSmem<D, NK, NV, false, false>::kAlloc, (int)fa::kTmemCols, out);
@@ -701,6 +777,8 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     bool ok = cudaEventRecord(hp->start, cs) == cudaSuccess && cudaStreamWaitEvent(hp->h2d, hp->start, 0) == cudaSuccess &&
               cudaStreamWaitEvent(hp->d2h, hp->start, 0) == cudaSuccess;
     const long long n_chunks = (BH + hc - 1) / hc;
+    // every chunk runs the kernel fa_fwd would choose for all B*H heads: same bits
+    const int two = use_two(d, causal ? 1 : 0, (N + fa::kBlockN - 1) / fa::kBlockN, BH) ? 1 : 0;
     for (long long c = 0; ok && c < n_chunks; ++c) {
         const int sl = (int)(c % kHostSlots);
         const long long h0 = c * hc;
@@ -725,7 +803,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
         Prepared pr;
         rc = prepare(dq, dk, dv, dout, dlse, 1, nh, N, d, causal, scale, &pr);
         if (rc != FA_OK) return rc;
-        rc = launch_d<false>(d, pr, cs);
+        rc = launch_d<false>(d, pr, cs, two);
         if (rc != FA_OK) return rc;
         // outputs
         ok = cudaEventRecord(hp->compute_done[sl], cs) == cudaSuccess &&
@@ -936,6 +1014,7 @@ int fa_fwd_kernel_for(int B, int H, int N, int d, int causal) {
     if (d != 64 && d != 128) return FA_ERR_HEAD_DIM;
     if (B < 1 || H < 1 || N < 1 || (long long)B * H > 65535) return FA_ERR_SHAPE;
     const int n_tiles = (N + fa::kBlockN - 1) / fa::kBlockN;
+    if (use_two(d, causal ? 1 : 0, n_tiles, (long long)B * H)) return FA_KERNEL_FWD_TWO;
     return use_pair(d, causal ? 1 : 0, n_tiles) ? FA_KERNEL_FWD_PAIR : FA_KERNEL_FWD;
 }
 

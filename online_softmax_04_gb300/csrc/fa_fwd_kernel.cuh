@@ -445,8 +445,11 @@ __device__ inline void tile_work(const FaParams& p, int bh, int qt, TileWork& w)
 //  * CTA pair: the leading CTA's producer chooses each unit and posts it in
 //    both CTAs' rings; every reader of either CTA releases the slot on the
 //    leading CTA's barrier.  Each CTA reads the unit as its own query tile.
-template <bool kSplit, bool kPersistent, bool kMask, bool kPair = false>
+//  * kTwo: units of two adjacent query tiles in one CTA (the two-tile kernel);
+//    the item names the unit's first tile.
+template <bool kSplit, bool kPersistent, bool kMask, bool kPair = false, bool kTwo = false>
 struct TileSeq {
+    static constexpr bool kUnits2 = kPair || kTwo;  // units of two query tiles
     int n = 0;               // items taken so far
     volatile int* ring;      // item ring in shared memory, 4 ints per entry
     uint32_t bar_full, bar_empty;
@@ -476,7 +479,7 @@ struct TileSeq {
     // producer (one thread): choose the next tile and post it
     int round = 0, sub = 0;  // static phase: pair round and tile within the pair
     __device__ bool choose(const FaParams& p, int& bh, int& qt) {
-        const int nu = schedule_units(p, kPair);
+        const int nu = schedule_units(p, kUnits2);
         const unsigned worker = kPair ? blockIdx.x >> 1 : blockIdx.x;
         const unsigned workers = kPair ? gridDim.x >> 1 : gridDim.x;
         if (p.static_rounds < 0) {
@@ -498,7 +501,7 @@ struct TileSeq {
             ++round;
         }
         const long long first = (long long)p.static_rounds * workers;  // first dynamic pair
-        const long long n_dyn = persistent_pairs(p, kPair) - first;
+        const long long n_dyn = persistent_pairs(p, kUnits2) - first;
         for (;;) {
             const long long k = (long long)atomicAdd(p.queue, 1u);
             if (k >= 2 * n_dyn) return false;
@@ -527,9 +530,9 @@ struct TileSeq {
             int bh = 0, qt = 0;
             const bool more = choose(p, bh, qt);
             if (more) {
-                if constexpr (kPair) {
-                    // unit qt: query tiles 2 qt (here) and 2 qt + 1 (peer) against every
-                    // key tile either of them sees
+                if constexpr (kUnits2) {
+                    // unit qt: query tiles 2 qt (here) and 2 qt + 1 (peer, or the second
+                    // tile of this CTA) against every key tile either of them sees
                     w.qt = 2 * qt;
                     w.bh = bh;
                     w.j0 = 0;
@@ -538,7 +541,7 @@ struct TileSeq {
                     tile_work<kMask>(p, bh, qt, w);  // the key range is worked out once, here
                 }
             }
-            const int e0 = more ? bh * schedule_units(p, kPair) + qt : -1, e1 = more ? w.j0 : 0, e2 = more ? w.n_kv : 0;
+            const int e0 = more ? bh * schedule_units(p, kUnits2) + qt : -1, e1 = more ? w.j0 : 0, e2 = more ? w.n_kv : 0;
             ring[4 * s + 0] = e0;
             ring[4 * s + 1] = e1;
             ring[4 * s + 2] = e2;
@@ -576,8 +579,8 @@ struct TileSeq {
             }
             ++n;
             if (item < 0) return false;
-            const int nu = schedule_units(p, kPair);
-            w.qt = kPair ? 2 * (item % nu) + (int)rank : item % nu;
+            const int nu = schedule_units(p, kUnits2);
+            w.qt = kUnits2 ? 2 * (item % nu) + (int)rank : item % nu;
             w.bh = item / nu;
             w.j0 = j0;
             w.n_kv = n_kv;

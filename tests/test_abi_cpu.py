@@ -41,11 +41,13 @@ def test_strerror_and_version(fa):
 
 
 def test_fwd_pairing_policy(fa):
-    """Which d = 128 forward kernel a call takes: CTA pairs for full attention and
+    """Which forward kernel a call takes.  d = 128: CTA pairs for full attention and
     for causal attention from 96 query tiles on (the masked key tile a pair
-    computes per two query tiles costs 1 / (tiles / 2 + 1)); d = 64 always one
-    CTA per tile; the override modes; host-only, no device touched."""
-    F, P = fa.FA_KERNEL_FWD, fa.FA_KERNEL_FWD_PAIR
+    computes per two query tiles costs 1 / (tiles / 2 + 1)).  d = 64: two tiles
+    per CTA once there are enough units to fill the SMs (not for one head of
+    N = 4096, nor for many heads of two tiles, where the masked tile is a third
+    of the work).  The override modes; host-only, no device touched."""
+    F, P, T = fa.FA_KERNEL_FWD, fa.FA_KERNEL_FWD_PAIR, fa.FA_KERNEL_FWD_TWO
     prev = fa.fa_set_fwd_pairing(fa.FA_PAIR_AUTO)
     try:
         assert fa.fa_fwd_kernel_for(1, 32, 16384, 128, True) == P      # 128 tiles
@@ -54,13 +56,19 @@ def test_fwd_pairing_policy(fa):
         assert fa.fa_fwd_kernel_for(4, 16, 4096, 128, True) == F
         assert fa.fa_fwd_kernel_for(1, 1, 1, 128, False) == P
         assert fa.fa_fwd_kernel_for(4, 16, 4096, 128, False) == P
-        assert fa.fa_fwd_kernel_for(1, 8, 131072, 64, True) == F
-        assert fa.fa_fwd_kernel_for(1, 1, 4096, 64, False) == F
+        assert fa.fa_fwd_kernel_for(1, 8, 131072, 64, True) == T
+        assert fa.fa_fwd_kernel_for(4, 16, 4096, 64, True) == T
+        assert fa.fa_fwd_kernel_for(2, 16, 8192, 64, False) == T
+        assert fa.fa_fwd_kernel_for(1, 1, 4096, 64, False) == F      # 16 units on 152 SMs
+        assert fa.fa_fwd_kernel_for(1, 4, 4096, 64, False) == F
+        assert fa.fa_fwd_kernel_for(32, 32, 256, 64, True) == F     # two tiles a head
+        assert fa.fa_fwd_kernel_for(1, 1, 256, 64, False) == F
         assert fa.fa_set_fwd_pairing(fa.FA_PAIR_OFF) == fa.FA_PAIR_AUTO
         assert fa.fa_fwd_kernel_for(1, 1, 4096, 128, False) == F
+        assert fa.fa_fwd_kernel_for(1, 8, 131072, 64, True) == F
         assert fa.fa_set_fwd_pairing(fa.FA_PAIR_ON) == fa.FA_PAIR_OFF
         assert fa.fa_fwd_kernel_for(1, 1, 256, 128, True) == P
-        assert fa.fa_fwd_kernel_for(1, 1, 256, 64, True) == F
+        assert fa.fa_fwd_kernel_for(1, 1, 256, 64, True) == T
         assert fa.lib().fa_fwd_kernel_for(1, 1, 256, 96, 0) == fa.FA_ERR_HEAD_DIM
         assert fa.lib().fa_fwd_kernel_for(0, 1, 256, 128, 0) == fa.FA_ERR_SHAPE
         assert fa.lib().fa_fwd_kernel_for(300, 300, 256, 128, 0) == fa.FA_ERR_SHAPE

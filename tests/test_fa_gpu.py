@@ -37,7 +37,8 @@ def fa():
 
 @contextlib.contextmanager
 def pairing(fa, mode):
-    """Force the d = 128 forward kernel (one CTA per tile, or CTA pairs) for the block."""
+    """Force the forward kernel for the block: one query tile per CTA (OFF), or pairs of
+    adjacent query tiles (ON: CTA pairs at d = 128, two tiles in one CTA at d = 64)."""
     prev = fa.fa_set_fwd_pairing(mode)
     try:
         yield
@@ -95,16 +96,22 @@ def test_small_shapes_every_row(fa, B, H, N, d, causal):
     compare(o, lse, q, k, v, causal, w.scale, all_rows(B, H, N), f"B{B} H{H} N{N} d{d} causal={causal}")
 
 
+def paired_kind(fa, d):
+    return fa.FA_KERNEL_FWD_PAIR if d == 128 else fa.FA_KERNEL_FWD_TWO
+
+
 @pytest.mark.parametrize("mode", [OFF, ON])
-@pytest.mark.parametrize("B,H,N,d,causal", [s for s in SMALL if s[3] == 128] + [(1, 3, 640, 128, True), (2, 2, 383, 128, False)])
-def test_small_shapes_each_d128_kernel(fa, mode, B, H, N, d, causal):
-    """Both d = 128 forward kernels on every small shape, every row: one CTA per
-    query tile, and CTA pairs (odd tile counts leave the peer of the last pair
-    past N; causal pairs compute a fully masked key tile for the first CTA)."""
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL + [(1, 3, 640, 128, True), (2, 2, 383, 128, False),
+                                                    (1, 3, 640, 64, True), (2, 2, 383, 64, False)])
+def test_small_shapes_each_kernel(fa, mode, B, H, N, d, causal):
+    """Both forward kernels of each head dim on every small shape, every row: one
+    query tile per CTA, and pairs of adjacent tiles (CTA pairs at d = 128, two
+    tiles per CTA at d = 64).  Odd tile counts leave the second tile of the last
+    pair past N; causal pairs compute a fully masked key tile for the first."""
     w = wl.Workload("small", B, H, N, d, causal, "iid", 100 + N + d)
     q, k, v = wl.make_inputs(w)
     with pairing(fa, mode):
-        assert fa.fa_fwd_kernel_for(B, H, N, d, causal) == (fa.FA_KERNEL_FWD_PAIR if mode == ON else fa.FA_KERNEL_FWD)
+        assert fa.fa_fwd_kernel_for(B, H, N, d, causal) == (paired_kind(fa, d) if mode == ON else fa.FA_KERNEL_FWD)
         o, lse = run_gpu(fa, q, k, v, causal, w.scale)
     compare(o, lse, q, k, v, causal, w.scale, all_rows(B, H, N), f"mode {mode} B{B} H{H} N{N} causal={causal}")
 
@@ -142,9 +149,30 @@ def test_random_shapes_both_d128_kernels(fa):
                 f"random B{B} H{H} N{N} causal={causal}")
 
 
+def test_random_shapes_both_d64_kernels(fa):
+    """Twelve seeded random d = 64 shapes (odd and even query-tile counts, ragged
+    tails, causal or not), each through both d = 64 forward kernels and compared
+    with the oracle on every row.  The two normalise O differently (the
+    tensor-core sum of the rounded weights; the fp32 sum with each tile's
+    largest-weight rounding), so they agree to rounding, not bit for bit."""
+    rng = np.random.default_rng(20261203)
+    for case in range(12):
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+        N = int(rng.integers(1, 1400))
+        causal = bool(rng.integers(0, 2))
+        w = wl.Workload(f"rand64-{case}", B, H, N, 64, causal, "iid", 700 + case)
+        q, k, v = wl.make_inputs(w)
+        for mode in (OFF, ON):
+            with pairing(fa, mode):
+                o, lse = run_gpu(fa, q, k, v, causal, w.scale)
+            compare(o, lse, q, k, v, causal, w.scale, all_rows(B, H, N),
+                    f"random d64 mode {mode} B{B} H{H} N{N} causal={causal}")
+
+
 @pytest.mark.parametrize("name,mode", [
     ("B4-H16-N4096-d128-causal", AUTO), ("B1-H32-N16384-d128-causal-late", AUTO), ("B1-H8-N131072-d64-causal", AUTO),
-    ("B4-H16-N4096-d128-causal", ON), ("B1-H32-N16384-d128-causal-late", OFF),
+    ("B4-H16-N4096-d128-causal", ON), ("B1-H32-N16384-d128-causal-late", OFF), ("B1-H8-N131072-d64-causal", ON),
+    ("B1-H8-N131072-d64-causal", OFF),
 ])
 def test_large_workloads_sampled_rows(fa, name, mode):
     """The full-size configurations in the kernel the default policy picks (the
@@ -156,8 +184,8 @@ def test_large_workloads_sampled_rows(fa, name, mode):
     compare(o, lse, q, k, v, w.causal, w.scale, wl.sample_rows(w), f"{name} mode {mode}")
 
 
-@pytest.mark.parametrize("d,causal,mode", [(64, True, AUTO), (64, False, AUTO), (128, True, OFF), (128, True, ON),
-                                           (128, False, AUTO)])
+@pytest.mark.parametrize("d,causal,mode", [(64, True, OFF), (64, False, OFF), (64, True, ON), (64, False, ON),
+                                           (128, True, OFF), (128, True, ON), (128, False, AUTO)])
 def test_reference_moves_often(fa, d, causal, mode):
     """Scores that grow steeply along the keys (q = 8 N(0,1), key norms ramping
     from 0.25 to 8.25 times N(0,1)): a row's running maximum outgrows its
@@ -347,12 +375,13 @@ def test_watchdog_ends_a_wait_nothing_completes(fa):
     assert fa.fa_get_last_error() == 0
 
 
-@pytest.mark.parametrize("d,mode", [(64, AUTO), (128, OFF), (128, ON)])
+@pytest.mark.parametrize("d,mode", [(64, OFF), (64, ON), (128, OFF), (128, ON)])
 def test_watchdog_abort_leaves_nan_lse(fa, d, mode):
     """The forward kernel's own abort path: its S products withheld, the softmax
     warps' first wait runs out; the tile's lse rows read NaN, o is not written,
-    and the context stays usable.  ON: a CTA pair, both CTAs abort (the peer's
-    query tile lies past N) and leave together."""
+    and the context stays usable.  ON at d = 128: a CTA pair, both CTAs abort
+    (the peer's query tile lies past N) and leave together; at d = 64 one CTA
+    with two tiles, the second past N."""
     N = 100
     w = wl.Workload("abort", 1, 1, N, d, False, "iid", 31)
     q, k, v = (t.cuda() for t in wl.make_inputs(w))
@@ -377,10 +406,9 @@ def test_kernel_resources_report(fa, d):
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     assert sm >= 1
     kernels = [fa.FA_KERNEL_FWD, fa.FA_KERNEL_FWD_MASKED, fa.FA_KERNEL_FWD_SPLITKV, fa.FA_KERNEL_BWD_DQ,
-               fa.FA_KERNEL_BWD_DKDV] + ([fa.FA_KERNEL_FWD_PAIR] if d == 128 else [])
-    if d == 64:
-        with pytest.raises(fa.FaError):
-            fa.fa_kernel_resources(64, fa.FA_KERNEL_FWD_PAIR)
+               fa.FA_KERNEL_BWD_DKDV, paired_kind(fa, d)]
+    with pytest.raises(fa.FaError):  # each paired kernel exists at one head dim only
+        fa.fa_kernel_resources(d, fa.FA_KERNEL_FWD_PAIR if d == 64 else fa.FA_KERNEL_FWD_TWO)
     for kernel in kernels:
         r = fa.fa_kernel_resources(d, kernel)
         assert r["threads_per_cta"] == 384, r

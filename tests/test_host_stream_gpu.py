@@ -41,6 +41,7 @@ CASES = [  # (B, H, N, d, causal, heads_per_chunk, pinned)
     (1, 2, 129, 64, False, 2, True),     # one chunk holds every head
     (1, 16, 2048, 128, True, 4, True),   # four chunks, several persistent rounds each
     (1, 7, 513, 64, True, 1, True),      # seven chunks: every one of the three slots reused
+    (4, 16, 4096, 64, True, 0, True),    # d = 64, 64 heads: two tiles per CTA, also in every 8-head chunk
 ]
 
 
