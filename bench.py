@@ -179,12 +179,23 @@ def strip_c_comments(text: str) -> str:
     return "".join(out)
 
 
-def kernel_source_hash() -> str:
-    """sha256 prefix of online_softmax_04_gb300/csrc/*, comments removed: a traffic record
-    stays valid across comment edits and lapses with any change to what compiles."""
+# the csrc/ files each profiled kernel compiles from (fa_fwd.cu holds every launcher)
+KERNEL_SOURCES = {
+    KERNEL_NAME: ("fa_fwd.cu", "fa_fwd_kernel.cuh", "fa_fwd_two_kernel.cuh", "sm103_ptx.cuh"),
+    "softmax_rows_smem": ("fa_fwd.cu", "softmax_rows.cuh", "sm103_ptx.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str = KERNEL_NAME) -> str:
+    """sha256 prefix of the csrc/ files `kernel` compiles from (all of them for a kernel not
+    listed), comments removed: a traffic record stays valid across comment edits and lapses
+    with any change to what the kernel compiles from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "online_softmax_04_gb300", "csrc")
+    names = KERNEL_SOURCES.get(kernel)
     for name in sorted(os.listdir(csrc)):
+        if names is not None and name not in names:
+            continue
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
             # lines left blank by the comments are dropped, so adding or removing a
@@ -199,7 +210,7 @@ def recorded_traffic(workload: str, kernel: str = KERNEL_NAME):
     path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     with open(path) as f:
         for line in f:
             parts = line.split()

@@ -99,7 +99,8 @@ struct BwdSmem {
     static constexpr int kBarFinal = kBarUsed + 2;      // the accumulators are complete
     static constexpr int kBarDrain = kBarFinal + 1;     // [2] per MMA issuer
     static constexpr int kBarSRead = kBarDrain + 2;     // [2] dQ kernel: the compute warps hold S / dP in registers
-    static constexpr int kNumBars = kBarSRead + 2;
+    static constexpr int kBarPHalf = kBarSRead + 2;     // dK/dV kernel, d = 128: half of each warp's P^T written
+    static constexpr int kNumBars = kBarPHalf + 1;
     static constexpr uint32_t kOffStage = kOffBar + kNumBars * 8;     // [8 warps][2][LSE 128, D 128] floats
     static constexpr uint32_t kOffTmemSlot = kOffStage + 8 * 2 * 256 * 4;
     static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
@@ -453,6 +454,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(L::kBarDrain + 1), 1);
         mbar_init(bar(L::kBarSRead + 0), 8);  // S^T in registers (separate operand columns only)
         mbar_init(bar(L::kBarSRead + 1), 8);  // dP^T in registers
+        mbar_init(bar(L::kBarPHalf), 8);      // the first 32 queries of each warp's P^T written (d = 128)
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tensormap(&tm_q);
@@ -594,19 +596,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tc_commit(bar(L::kBarSFull + u));
                     }
                     __syncwarp();
-                    // its bf16 operand: P^T (written first) or dS^T
-                    ok = fa_wait_warp(bar(L::kBarDSFull + u), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
-                    if (!ok) break;
-                    tc_fence_after_sync();
                     // the bf16 operands of queries 16 kk .. 16 kk + 15 sit at column 8 kk (first
                     // half of the queries) or 32 + 8 kk (second half); the B rows advance 2048
                     // bytes per 16 queries
                     const uint64_t gd = sdesc_sw128(b_acc, kChunkBytes, 1024);
+                    auto grad_mma = [&](int kk) {
+                        mma_ts(tmem + col_acc, tmem + col_sc + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
+                               sdesc_add_lo(gd, (uint32_t)kk * 128u), kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+                    };
+                    if (u == 0) {
+                        // dV in two halves: queries 0-31 and 64-95 (each warp's first 32 columns
+                        // of P^T) as soon as those are written, while the rest is formed
+                        ok = fa_wait_warp(bar(L::kBarPHalf), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        if (elect_one_sync()) {
+                            grad_mma(0);
+                            grad_mma(1);
+                            grad_mma(4);
+                            grad_mma(5);
+                        }
+                        __syncwarp();
+                    }
+                    // its bf16 operand: P^T (written first) or dS^T
+                    ok = fa_wait_warp(bar(L::kBarDSFull + u), (uint32_t)(i & 1), abort_flag, limit, kStatusMmaWaitP);
+                    // dK(i) after S^T(i+1) has finished: the pipe interleaves the two issuers'
+                    // products, so issued beside S^T(i+1) it would double the latency of the
+                    // product the compute warps wait for next
+                    if (ok && u == 1 && i + 1 < n_q)
+                        ok = fa_wait_warp(bar(L::kBarSFull + 0), (uint32_t)((i + 1) & 1), abort_flag, limit,
+                                          kStatusMmaWaitP);
+                    if (!ok) break;
+                    tc_fence_after_sync();
                     if (elect_one_sync()) {
+                        if (u == 0) {
+                            grad_mma(2);
+                            grad_mma(3);
+                            grad_mma(6);
+                            grad_mma(7);
+                        } else {
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ts(tmem + col_acc, tmem + col_sc + (uint32_t)kk * 8u + (kk >= 4 ? 32u : 0u),
-                                   sdesc_add_lo(gd, (uint32_t)kk * 128u), kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < 8; ++kk) grad_mma(kk);
+                        }
                         tc_commit(bar(L::kBarEmpty + s));
                         tc_commit(bar(L::kBarUsed + u));
                     }
@@ -718,6 +749,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int i2 = 0; i2 < 16; ++i2) pk[i2] = pack_bf16x2(pf[32 * hc + 2 * i2], pf[32 * hc + 2 * i2 + 1]);
                 tmem_st16(t_lane + kColOp0 + op_off + 16u * hc, pk);
+                if (!kSepOp && hc == 0) {  // the first half of the dV product may start
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (elect_one_sync()) mbar_arrive(bar(L::kBarPHalf));
+                }
             }
             tmem_st_wait();
             tc_fence_before_sync();

@@ -100,8 +100,29 @@ def test_source_hash_ignores_comment_lines(tmp_path, monkeypatch):
     f = src / "k.cuh"
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     f.write_text("int a = 1;\nint b = 2;\n")
-    h0 = bench.kernel_source_hash()
+    h0 = bench.kernel_source_hash("k")  # a kernel with no source list: every file counts
     f.write_text("// header\n//   more\nint a = 1;  // one\n\n// note\nint b = 2;\n")
-    assert bench.kernel_source_hash() == h0
+    assert bench.kernel_source_hash("k") == h0
     f.write_text("int a = 1;\nint b = 3;\n")
+    assert bench.kernel_source_hash("k") != h0
+
+
+def test_forward_source_hash_covers_the_forward_files_only(tmp_path, monkeypatch):
+    """The forward's traffic records lapse with a change to the files its kernels compile
+    from, not with a change to the backward or row-softmax kernels."""
+    import bench
+
+    src = tmp_path / "online_softmax_04_gb300" / "csrc"
+    src.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    for name in ("fa_fwd.cu", "fa_fwd_kernel.cuh", "fa_fwd_two_kernel.cuh", "sm103_ptx.cuh", "fa_bwd_kernel.cuh",
+                 "softmax_rows.cuh"):
+        (src / name).write_text(f"int {name.split('.')[0]} = 0;\n")
+    h0 = bench.kernel_source_hash()
+    (src / "fa_bwd_kernel.cuh").write_text("int changed = 1;\n")
+    (src / "softmax_rows.cuh").write_text("int changed = 2;\n")
+    assert bench.kernel_source_hash() == h0
+    s0 = bench.kernel_source_hash("softmax_rows_smem")
+    (src / "fa_fwd_two_kernel.cuh").write_text("int changed = 3;\n")
     assert bench.kernel_source_hash() != h0
+    assert bench.kernel_source_hash("softmax_rows_smem") == s0
