@@ -79,8 +79,8 @@ struct BwdParams {
     unsigned long long watchdog_ns;
 };
 
-// shared memory of the backward kernels: two resident tiles, a ring of NS
-// stages of two streamed tiles, barriers, per-warp LSE/D staging
+// shared memory of the dK/dV kernel: two resident tiles, a ring of NS stages of
+// two streamed tiles, barriers, per-warp LSE/D staging
 template <int D, int NS>
 struct BwdSmem {
     static constexpr int kChunks = D / 64;
@@ -109,6 +109,37 @@ struct BwdSmem {
     static_assert(kAlloc <= 232448u, "shared memory");
 };
 
+// shared memory of the dQ kernel: Q and dO resident, then separate rings of NK
+// key and NV value tiles.  K_j is read by S_j and, a whole step later, by the dQ
+// product; V_j only by dP_j.  So K needs the deeper ring: with one ring of K and V
+// stages the next K_{j+2} could only load once dQ_j had finished, and S_{j+2}
+// waited for that load.
+template <int D, int NK, int NV>
+struct DqSmem {
+    static constexpr uint32_t kTileBytes = 128u * D * 2u;
+    static constexpr uint32_t kOffRes = 0;                       // Q, dO
+    static constexpr uint32_t kOffK = 2 * kTileBytes;            // [NK] key tiles
+    static constexpr uint32_t kOffV = kOffK + NK * kTileBytes;   // [NV] value tiles
+    static constexpr uint32_t kOffBar = kOffV + NV * kTileBytes;
+    static constexpr int kBarRes = 0;                    // resident tiles landed
+    static constexpr int kBarKFull = 1;                  // [NK] key stage landed
+    static constexpr int kBarKEmpty = kBarKFull + NK;    // [NK] key stage read by S_j and dQ_j
+    static constexpr int kBarVFull = kBarKEmpty + NK;    // [NV]
+    static constexpr int kBarVEmpty = kBarVFull + NV;    // [NV] value stage read by dP_j
+    static constexpr int kBarSFull = kBarVEmpty + NV;    // [2] S_j / dP_j finished
+    static constexpr int kBarDSFull = kBarSFull + 2;     // dS_j written
+    static constexpr int kBarUsed = kBarDSFull + 1;      // [2] per dS buffer: its dQ product finished
+    static constexpr int kBarFinal = kBarUsed + 2;       // dQ complete
+    static constexpr int kBarDrain = kBarFinal + 1;      // [2] per MMA issuer
+    static constexpr int kBarSRead = kBarDrain + 2;      // [2] the compute warps hold S / dP in registers
+    static constexpr int kNumBars = kBarSRead + 2;
+    static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+    static constexpr uint32_t kBytes = kOffAbort + 4;
+    static constexpr uint32_t kAlloc = kBytes + 1024;
+    static_assert(kAlloc <= 232448u, "shared memory");
+};
+
 // loads of the 64-column chunks of a [128 rows][D] tile
 template <int D>
 __device__ __forceinline__ void bwd_load_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, int row0, int bh) {
@@ -122,12 +153,12 @@ __device__ __forceinline__ void bwd_load_tile(uint32_t dst, const CUtensorMap* m
 // [256+D+64, 256+D+128), alternating by step, so that dS(j) is formed while
 // the dQ product of dS(j-1) still reads the other buffer.
 // ---------------------------------------------------------------------------
-template <int D, int NS>
+template <int D, int NK, int NV>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_sm103(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdParams p) {
-    using L = BwdSmem<D, NS>;
+    using L = DqSmem<D, NK, NV>;
     constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
     static_assert(256 + D + 128 <= kTmemCols, "TMEM budget");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -145,9 +176,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp == 0 && lane == 0) {
         mbar_init(bar(L::kBarRes), 1);
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(bar(L::kBarFull + s), 1);
-            mbar_init(bar(L::kBarEmpty + s), 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(bar(L::kBarKFull + s), 1);
+            mbar_init(bar(L::kBarKEmpty + s), 1);  // the dQ product's commit
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(bar(L::kBarVFull + s), 1);
+            mbar_init(bar(L::kBarVEmpty + s), 1);  // the dP product's commit
         }
         mbar_init(bar(L::kBarSFull + 0), 1);  // S
         mbar_init(bar(L::kBarSFull + 1), 1);  // dP
@@ -175,8 +210,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const uint32_t res_q = sbase + L::kOffRes, res_do = sbase + L::kOffRes + L::kTileBytes;
-    auto ring_k = [&](int s) { return sbase + L::kOffRing + (uint32_t)(2 * s) * L::kTileBytes; };
-    auto ring_v = [&](int s) { return sbase + L::kOffRing + (uint32_t)(2 * s + 1) * L::kTileBytes; };
+    auto ring_k = [&](int s) { return sbase + L::kOffK + (uint32_t)s * L::kTileBytes; };
+    auto ring_v = [&](int s) { return sbase + L::kOffV + (uint32_t)s * L::kTileBytes; };
 
     if (warp == 0) {
         // the whole warp walks the loop; one elected lane issues the copies
@@ -188,24 +223,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwd_load_tile<D>(res_do, &tm_do, bar(L::kBarRes), qt * 128, bh);
             }
             __syncwarp();
-            int j = 0;
-            for (; ok && j < n_kv; ++j) {
-                const int s = j % NS;
-                if (j >= NS)
-                    ok = fa_wait_warp(bar(L::kBarEmpty + s), (uint32_t)(((j - NS) / NS) & 1), abort_flag, limit,
+            int nk = 0, nv = 0;  // key and value tiles loaded
+            while (ok && nk < n_kv) {
+                const int j = nk;
+                const int sk = j % NK, sv = j % NV;
+                if (j >= NK)
+                    ok = fa_wait_warp(bar(L::kBarKEmpty + sk), (uint32_t)(((j - NK) / NK) & 1), abort_flag, limit,
                                       kStatusLoadWait);
                 if (!ok) break;
                 if (elect_one_sync()) {
-                    mbar_arrive_expect_tx(bar(L::kBarFull + s), 2 * L::kTileBytes);
-                    bwd_load_tile<D>(ring_k(s), &tm_k, bar(L::kBarFull + s), j * 128, bh);
-                    bwd_load_tile<D>(ring_v(s), &tm_v, bar(L::kBarFull + s), j * 128, bh);
+                    mbar_arrive_expect_tx(bar(L::kBarKFull + sk), L::kTileBytes);
+                    bwd_load_tile<D>(ring_k(sk), &tm_k, bar(L::kBarKFull + sk), j * 128, bh);
                 }
                 __syncwarp();
+                ++nk;
+                if (j >= NV)
+                    ok = fa_wait_warp(bar(L::kBarVEmpty + sv), (uint32_t)(((j - NV) / NV) & 1), abort_flag, limit,
+                                      kStatusLoadWait);
+                if (!ok) break;
+                if (elect_one_sync()) {
+                    mbar_arrive_expect_tx(bar(L::kBarVFull + sv), L::kTileBytes);
+                    bwd_load_tile<D>(ring_v(sv), &tm_v, bar(L::kBarVFull + sv), j * 128, bh);
+                }
+                __syncwarp();
+                ++nv;
             }
             if (lane == 0 && (!ok || *abort_flag)) {  // let every issued copy land before the CTA exits
                 fa_wait_drain(bar(L::kBarRes), 0, limit);
-                for (int s = 0; s < NS; ++s)
-                    if (j > s) fa_wait_drain(bar(L::kBarFull + s), (uint32_t)(((j - 1 - s) / NS) & 1), limit);
+                for (int s = 0; s < NK; ++s)
+                    if (nk > s) fa_wait_drain(bar(L::kBarKFull + s), (uint32_t)(((nk - 1 - s) / NK) & 1), limit);
+                for (int s = 0; s < NV; ++s)
+                    if (nv > s) fa_wait_drain(bar(L::kBarVFull + s), (uint32_t)(((nv - 1 - s) / NV) & 1), limit);
             }
         }
         __syncwarp();
@@ -219,14 +267,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t qd = sdesc_sw128(res_q, 16, 1024), dod = sdesc_sw128(res_do, 16, 1024);
             bool ok = fa_wait_warp(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
             for (int j = 0; ok && j < n_kv; ++j) {
-                const int s = j % NS;
-                ok = fa_wait_warp(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit, kStatusMmaWaitK);
+                const int sk = j % NK, sv = j % NV;
+                ok = fa_wait_warp(bar(L::kBarKFull + sk), (uint32_t)((j / NK) & 1), abort_flag, limit, kStatusMmaWaitK);
                 if (ok && j > 0)
                     ok = fa_wait_warp(bar(L::kBarSRead + 0), (uint32_t)((j - 1) & 1), abort_flag, limit,
                                       kStatusMmaWaitSFree);
                 if (!ok) break;
                 tc_fence_after_sync();
-                const uint64_t kd = sdesc_sw128(ring_k(s), 16, 1024), vd = sdesc_sw128(ring_v(s), 16, 1024);
+                const uint64_t kd = sdesc_sw128(ring_k(sk), 16, 1024), vd = sdesc_sw128(ring_v(sv), 16, 1024);
                 if (elect_one_sync()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -236,7 +284,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tc_commit(bar(L::kBarSFull + 0));
                 }
                 __syncwarp();
-                if (j > 0)
+                ok = fa_wait_warp(bar(L::kBarVFull + sv), (uint32_t)((j / NV) & 1), abort_flag, limit, kStatusMmaWaitV);
+                if (ok && j > 0)
                     ok = fa_wait_warp(bar(L::kBarSRead + 1), (uint32_t)((j - 1) & 1), abort_flag, limit,
                                       kStatusMmaWaitSFree);
                 if (!ok) break;
@@ -249,6 +298,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bar(L::kBarSFull + 1));
+                    tc_commit(bar(L::kBarVEmpty + sv));  // V_j is read by dP_j only
                 }
                 __syncwarp();
             }
@@ -265,8 +315,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, false, true);
             bool ok = fa_wait_warp(bar(L::kBarRes), 0, abort_flag, limit, kStatusMmaWaitQ);
             for (int j = 0; ok && j < n_kv; ++j) {
-                const int s = j % NS;
-                ok = fa_wait_warp(bar(L::kBarFull + s), (uint32_t)((j / NS) & 1), abort_flag, limit,
+                const int s = j % NK;
+                ok = fa_wait_warp(bar(L::kBarKFull + s), (uint32_t)((j / NK) & 1), abort_flag, limit,
                                   kStatusMmaWaitK) &&
                      fa_wait_warp(bar(L::kBarDSFull), (uint32_t)(j & 1), abort_flag, limit, kStatusMmaWaitP);
                 if (!ok) break;
@@ -277,9 +327,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ts(tmem + kColDQ, tmem + kColDS + 64u * (uint32_t)(j & 1) + (uint32_t)kk * 8u,
                                sdesc_add_lo(kd, (uint32_t)kk * 128u), kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
-                    // S_j and dP_j finished before dS_j was written, so this covers every
-                    // product that read stage s
-                    tc_commit(bar(L::kBarEmpty + s));
+                    // S_j finished before dS_j was written, so this covers both products
+                    // that read K_j
+                    tc_commit(bar(L::kBarKEmpty + s));
                     tc_commit(bar(L::kBarUsed + (j & 1)));
                 }
                 __syncwarp();

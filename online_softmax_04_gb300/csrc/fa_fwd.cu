@@ -440,6 +440,13 @@ int bwd_pipe(BwdPipe** out) {
     return FA_OK;
 }
 
+// key and value stages of the dQ kernel: at d = 128, 3 K + 2 V stages of 32 KB
+// (K is read again by the dQ product a step after S); at d = 64, 4 + 4 of 16 KB
+template <int D>
+struct DqStages {
+    static constexpr int NK = D == 64 ? 4 : 3, NV = D == 64 ? 4 : 2;
+};
+
 template <int D, int NS>
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                const void* o, const void* dout, float* delta, void* dq, void* dk, void* dv, fa::BwdParams p, int BH,
@@ -449,9 +456,10 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
     fa::fa_bwd_delta<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
                                                                       static_cast<const __nv_bfloat16*>(dout), delta,
                                                                       rows);
-    auto kq = fa::fa_bwd_dq_sm103<D, NS>;
+    using LQ = fa::DqSmem<D, DqStages<D>::NK, DqStages<D>::NV>;
+    auto kq = fa::fa_bwd_dq_sm103<D, DqStages<D>::NK, DqStages<D>::NV>;
     auto kkv = fa::fa_bwd_dkdv_sm103<D, NS>;
-    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess ||
+    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LQ::kAlloc) != cudaSuccess ||
         cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kAlloc) != cudaSuccess)
         return FA_ERR_CUDA;
     const dim3 grid((unsigned)p.n_tiles, (unsigned)BH);
@@ -469,7 +477,7 @@ int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
     kkv<<<grid, fa::kBwdThreads, L::kAlloc, bp->side>>>(tq, tk, tv, tdo, p);
     p.grad = dq;
     p.grad2 = nullptr;
-    kq<<<grid, fa::kBwdThreads, L::kAlloc, st>>>(tq, tk, tv, tdo, p);
+    kq<<<grid, fa::kBwdThreads, LQ::kAlloc, st>>>(tq, tk, tv, tdo, p);
     // the caller's stream continues once both have finished
     if (cudaEventRecord(bp->kv_done, bp->side) != cudaSuccess || cudaStreamWaitEvent(st, bp->kv_done, 0) != cudaSuccess)
         return FA_ERR_CUDA;
@@ -581,8 +589,8 @@ int fwd_resources(int kernel, fa_kernel_resources_t* out) {
             return kernel_resources(fa::fa_fwd_sm103<D, NK, NV, true, false, false>, fa::kThreads,
                                     fa::FwdSmem<D, NK, NV, true, false>::kAlloc, (int)fa::kTmemCols, out);
         case FA_KERNEL_BWD_DQ:
-            return kernel_resources(fa::fa_bwd_dq_sm103<D, D == 64 ? 4 : 2>, fa::kBwdThreads,
-                                    fa::BwdSmem<D, D == 64 ? 4 : 2>::kAlloc, (int)fa::kTmemCols, out);
+            return kernel_resources(fa::fa_bwd_dq_sm103<D, DqStages<D>::NK, DqStages<D>::NV>, fa::kBwdThreads,
+                                    fa::DqSmem<D, DqStages<D>::NK, DqStages<D>::NV>::kAlloc, (int)fa::kTmemCols, out);
         case FA_KERNEL_BWD_DKDV:
             return kernel_resources(fa::fa_bwd_dkdv_sm103<D, D == 64 ? 4 : 2>, fa::kBwdThreads,
                                     fa::BwdSmem<D, D == 64 ? 4 : 2>::kAlloc, (int)fa::kTmemCols, out);
