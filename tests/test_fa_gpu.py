@@ -261,7 +261,8 @@ def test_work_queue_across_calls_and_streams(fa, mode):
     launch leaves at zero: back-to-back calls, and calls overlapping on two
     streams, must give exactly the results of the same calls run alone (every
     tile's arithmetic is independent of which CTA runs it).  ON: the d = 128
-    calls run in CTA pairs (128 two-tile units: static rounds + dynamic tail)."""
+    calls run in CTA pairs (128 two-tile units: static rounds + dynamic tail),
+    the d = 64 calls two tiles per CTA (48 units, one CTA each)."""
     with pairing(fa, mode):
         _work_queue_calls(fa)
 
@@ -291,7 +292,7 @@ def _work_queue_calls(fa):
         assert torch.equal(o, ro) and torch.equal(l, rl), which
 
 
-@pytest.mark.parametrize("d,mode", [(64, AUTO), (128, OFF), (128, ON)])
+@pytest.mark.parametrize("d,mode", [(64, OFF), (64, ON), (128, OFF), (128, ON)])
 def test_output_alignment_and_bounds(fa, d, mode):
     """O at a 16-byte but not 32-byte aligned address, N ragged: the same values
     as an aligned output, and nothing written outside O (rows past N are not
@@ -320,7 +321,8 @@ def _aligned_and_bounded(fa, q, k, v, B, H, N, d):
     assert torch.all(buf[:pad + 8] == -7.0) and torch.all(buf[pad + 8 + n:] == -7.0)
 
 
-@pytest.mark.parametrize("B,H,N,d,mode", [(1, 65535, 3, 64, AUTO), (65535, 1, 40, 128, OFF), (65535, 1, 40, 128, ON)])
+@pytest.mark.parametrize("B,H,N,d,mode", [(1, 65535, 3, 64, OFF), (1, 65535, 3, 64, ON), (65535, 1, 40, 128, OFF),
+                                         (65535, 1, 40, 128, ON)])
 def test_largest_head_count(fa, B, H, N, d, mode):
     """B*H at the limit the boundary accepts (65535): every (head, query tile)
     unit runs through the persistent schedule's static rounds and dynamic tail;
@@ -420,18 +422,20 @@ def test_kernel_resources_report(fa, d):
 
 
 @pytest.mark.parametrize("heads,d,causal", [(None, 64, False), ("sm+1", 64, False), (None, 128, True),
-                                           ("pairs", 128, True), ("pairs+1", 128, True)])
+                                           ("pairs", 128, True), ("pairs+1", 128, True), ("units", 64, True),
+                                           ("units+1", 64, False)])
 def test_one_tile_per_cta_boundary(fa, heads, d, causal):
     """N = 128, so each head is one query tile: as many heads as SMs gives each CTA
     its tile by index; one more head takes the persistent schedule with its work
     counter.  CTA pairs (N = 256, one two-tile unit per head): as many heads as
-    pairs fit on the device (one per two SMs), and one more.  Every row against
+    pairs fit on the device (one per two SMs), and one more.  Two tiles per CTA
+    (d = 64, N = 256): as many units as SMs, and one more.  Every row against
     the oracle."""
     sm = torch.cuda.get_device_properties(0).multi_processor_count
-    H = {"sm+1": sm + 1, "pairs": sm // 2, "pairs+1": sm // 2 + 1}.get(heads, sm)
-    N = 256 if heads and heads.startswith("pairs") else 128
+    H = {"sm+1": sm + 1, "pairs": sm // 2, "pairs+1": sm // 2 + 1, "units": sm, "units+1": sm + 1}.get(heads, sm)
+    N = 256 if heads and heads.startswith(("pairs", "units")) else 128
     w = wl.Workload(f"tiles-{H}", 1, H, N, d, causal, "iid", 61 + H)
     q, k, v = wl.make_inputs(w)
-    with pairing(fa, ON if N == 256 else AUTO):
+    with pairing(fa, ON if N == 256 else OFF):
         o, lse = run_gpu(fa, q, k, v, causal, w.scale)
     compare(o, lse, q, k, v, causal, w.scale, all_rows(1, H, N), w.name)
