@@ -16,8 +16,10 @@
 // for the other: a group hands no reference maximum across, and its P V
 // product waits only for its own previous one.  The one-tile kernel instead
 // splits one tile's steps between its two groups, which then wait on each
-// other every step; at d = 64, where a step has only 576 tensor-pipe cycles
-// of products against 512 cycles of exponentials, those waits set the step.
+// other every step; at d = 64, where a step's products (12 tensor-core
+// instructions of ~64 cycles: an N = 64 instruction costs what an N = 128 one
+// does) are not much longer than its 512 cycles of exponentials, those waits
+// set the step.
 //
 // Per tile and key step g (counted over the CTA's whole sequence):
 //   issuer:  S_g = Q K_g^T once the group has read S_{g-1} out of TMEM, then
@@ -32,7 +34,7 @@
 // tile, the bf16 rounding of the tile's largest weight.
 //
 // Causal units: tile A does not see key tile 2u + 1; its step there is fully
-// masked (weights 0), one wasted step in 4u + 3.  A unit past the last query
+// masked (weights 0), one wasted step in 4u + 4.  A unit past the last query
 // tile's partner (odd tile count) loads a real tile for B and never stores
 // its rows.
 #pragma once
